@@ -1,0 +1,458 @@
+"""Benchmark of the GB300 mixture-of-experts layer step.
+
+One step = the whole hot path on one batch: router scoring + top-k + capacity
+slotting, permute, grouped SwiGLU FFN (up and down), unpermute + combine, and
+the backward (combine backward, dgrad, wgrad with fp32 accumulation, dx +
+router gradient).  Default workload: the top-2 layer (T=4096, d=1024, f=4096,
+E=8, k=2, capacity factor 1.25) in bf16 with an fp32 router.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own batch
+(data-parallel replicas, weak scaling) and the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "top2_e8_bf16"
+METRIC = "MoE-layer tokens/s fwd & fwd+bwd; grouped-GEMM % bf16 peak; permute GB/s"
+PROFILE_FILE = os.path.join(ROOT, "profiles", "traffic_top2_e8_bf16.txt")
+KERNEL_SOURCES = {
+    "gemm_up_swiglu": "gemm_tc.cu", "gemm_down": "gemm_tc.cu", "gemm_dgrad_h_swiglu_bwd": "gemm_tc.cu",
+    "gemm_dgrad_x": "gemm_tc.cu", "gemm_wgrad": "gemm_tc.cu", "permute": "rows.cu", "unpermute_combine": "rows.cu",
+    "combine_bwd": "rows.cu", "dx_router": "rows.cu", "router_topk": "routing.cu",
+}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------------------- #
+# distributed plumbing
+# ----------------------------------------------------------------------------- #
+def dist_init(args):
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- #
+# clocks during the timed region
+# ----------------------------------------------------------------------------- #
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"moe_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sms, maxes, reasons, power = [], [], set(), []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, v in zip(self.NAMES, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sms) if sms else None, "sm_max_mhz": max(maxes) if maxes else None,
+                "reasons": sorted(reasons), "samples": len(sms),
+                "power_w_max": max(power) if power else None}
+
+
+# ----------------------------------------------------------------------------- #
+# algorithmic work per kernel (per launch)
+# ----------------------------------------------------------------------------- #
+def algorithmic_work(s, N: int):
+    """(unit, amount) per launch: FLOPs for the GEMMs, bytes for the row moves."""
+    T, d, f, E, k = s.T, s.d_model, s.d_ff, s.E, s.k
+    es = 2 if s.dtype == "bf16" else 4
+    return {
+        "router_topk": ("bytes", T * d * es + d * E * 4 + T * k * 8 + T * E * 4),
+        "permute": ("bytes", T * d * es + N * d * es),
+        "gemm_up_swiglu": ("flops", 4 * N * d * f),
+        "gemm_down": ("flops", 2 * N * f * d),
+        "unpermute_combine": ("bytes", N * d * es + T * d * es),
+        "combine_bwd": ("bytes", T * d * es + 2 * N * d * es + T * E * 4),
+        "gemm_dgrad_h_swiglu_bwd": ("flops", 2 * N * d * f),
+        "gemm_wgrad": ("flops", 6 * N * d * f),
+        "gemm_dgrad_x": ("flops", 4 * N * f * d),
+        "dx_router": ("bytes", N * d * es + T * d * es),
+    }
+
+
+def source_digest(name: str) -> str:
+    path = os.path.join(ROOT, "routing_permute_grouped_router_gb300", "csrc", KERNEL_SOURCES.get(name, "gemm_tc.cu"))
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def committed_traffic(name: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current source."""
+    if not os.path.exists(PROFILE_FILE):
+        return None
+    vals = {}
+    for line in open(PROFILE_FILE):
+        if ":" in line and line.strip().startswith("traffic."):
+            key, v = line.strip().split(":", 1)
+            vals[key.strip()] = v.strip()
+    tb = vals.get(f"traffic.{name}.bytes_per_launch")
+    sha = vals.get(f"traffic.{name}.source_sha")
+    if tb is None or sha != source_digest(name):
+        return None
+    return float(tb)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        pk = json.load(open(path))
+        return pk.get("hbm_gbs", 6800.0), pk.get("bf16_tflops_sustained", 1700.0), "measured"
+    return 6800.0, 1700.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- #
+# CPU oracle leg (a separate spawned process: numpy threads known, no fork after CUDA)
+# ----------------------------------------------------------------------------- #
+CPU_SNIPPET = r"""
+import json, sys, time
+sys.path.insert(0, {root!r})
+import numpy as np
+from oracle import moe_oracle as O
+from routing_permute_grouped_router_gb300 import workload as W
+shape = W.WORKLOADS[{name!r}].replace(T={tokens})
+wl = W.make(shape, seed=0, micro_batches=1, with_dy=True)
+C = O.capacity(shape.T, shape.k, shape.E, shape.capacity_factor, shape.capacity)
+args = (wl.W_r, wl.bias, wl.W1.f64(), wl.W3.f64(), wl.W2.f64())
+x, dy = wl.x[0].f64(), wl.dy[0].f64()
+times = []
+t_end = time.time() + {seconds}
+for rep in range({reps}):
+    t0 = time.perf_counter()
+    st = O.forward(x, *args, shape.k, C)
+    O.backward(dy, x, wl.W_r, args[2], args[3], args[4], st)
+    times.append(time.perf_counter() - t0)
+    if time.time() > t_end:
+        break
+print(json.dumps(dict(tokens={tokens}, times=times)))
+"""
+
+
+def run_oracle(name: str, tokens: int, seconds: float, reps: int, threads: int) -> dict:
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[v] = str(threads)
+    code = CPU_SNIPPET.format(root=ROOT, name=name, tokens=tokens, seconds=seconds, reps=reps)
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=1800)
+    if out.returncode != 0:
+        raise RuntimeError(out.stderr[-2000:])
+    return json.loads(out.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline(name: str, T: int, seconds: float) -> dict:
+    cores = len(os.sched_getaffinity(0))
+    probe = run_oracle(name, min(T, 512), 0, 1, cores)
+    per_tok = probe["times"][0] / probe["tokens"]
+    tokens = int(max(256, min(T, (seconds / 2) / max(per_tok, 1e-9))))
+    res = run_oracle(name, tokens, seconds, 50, cores)
+    t = statistics.median(res["times"])
+    return {"value": tokens / t, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"fp64 numpy oracle, forward+backward over the first {tokens} of the {T} tokens "
+                      f"(capacity factor applied to the sample), median of {len(res['times'])} runs, "
+                      f"BLAS threads = {cores}"}
+
+
+# ----------------------------------------------------------------------------- #
+# reference arm: the oracle as it stands
+# ----------------------------------------------------------------------------- #
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    from routing_permute_grouped_router_gb300 import workload as W
+
+    s = W.WORKLOADS[args.workload]
+    cores = len(os.sched_getaffinity(0))
+    probe = run_oracle(args.workload, min(s.T, 256), 0, 1, cores)
+    per_tok = probe["times"][0] / probe["tokens"]
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    tokens = int(max(16, min(s.T, budget / max(per_tok, 1e-9))))
+    res = run_oracle(args.workload, tokens, 1e9, args.steps + args.warmup, cores)
+    times = res["times"][args.warmup:] or res["times"]
+    total = sum(times)
+    value = tokens * len(times) / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": len(times), "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "T": s.T, "d_model": s.d_model, "d_ff": s.d_ff, "E": s.E, "k": s.k,
+                   "capacity_factor": s.capacity_factor, "sample_tokens": tokens},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: fp64 oracle forward+backward over the first {tokens} of {s.T} tokens"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- #
+# our arm
+# ----------------------------------------------------------------------------- #
+def run_ours(args, world, rank, local):
+    import torch
+
+    import routing_permute_grouped_router_gb300 as pkg
+    from routing_permute_grouped_router_gb300 import build as B
+    from routing_permute_grouped_router_gb300 import layer
+    from routing_permute_grouped_router_gb300 import workload as W
+
+    if not os.path.exists(pkg.LIB_PATH):
+        B.build()
+    pkg.lib()
+    dev = torch.device("cuda", local)
+    s = W.WORKLOADS[args.workload]
+    wl = W.make(s, seed=rank, micro_batches=1, with_dy=True)
+    L = layer.from_workload(wl, str(dev))
+    x = wl.x[0].torch(dev)
+    dy = wl.dy[0].torch(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)  # 2x the 129 MB L2
+
+    def step(accumulate=True):
+        L.forward(x)
+        L.backward(x, dy, accumulate=accumulate)
+
+    for i in range(max(3, args.warmup)):
+        step(accumulate=i > 0)
+    torch.cuda.synchronize(dev)
+    code, detail = pkg.moe_get_device_error(clear=True)
+    if code != 0:
+        raise RuntimeError(f"device error {code} {detail:#x}")
+    N = int(L.saved["counts"].sum().item())
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    n0 = pkg.moe_launch_count()
+    pkg.moe_profiler_enable(True)
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    pkg.moe_profiler_enable(False)
+    launches = pkg.moe_launch_count() - n0
+    barrier(world)
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_ms = max_over_ranks(sum(step_ms), world)
+    prof = pkg.moe_profiler_read()
+
+    # forward-only throughput (separate loop, same protocol)
+    fs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    fe = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        fs[i].record(stream)
+        L.forward(x)
+        fe[i].record(stream)
+    torch.cuda.synchronize(dev)
+    fwd_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(fs, fe)), world)
+
+    # end to end through host buffers: pinned x, dy in; y, dx out
+    e2e = None
+    if not args.no_e2e:
+        hx = x.cpu().pin_memory()
+        hdy = dy.cpu().pin_memory()
+        hy = torch.empty_like(L.y, device="cpu").pin_memory()
+        hdx = torch.empty_like(L.dx, device="cpu").pin_memory()
+        dx_in = torch.empty_like(x)
+        dy_in = torch.empty_like(dy)
+        for _ in range(2):
+            dx_in.copy_(hx, non_blocking=True)
+            dy_in.copy_(hdy, non_blocking=True)
+            L.forward(dx_in)
+            L.backward(dx_in, dy_in, accumulate=True)
+            hy.copy_(L.y, non_blocking=True)
+            hdx.copy_(L.dx, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            dx_in.copy_(hx, non_blocking=True)
+            dy_in.copy_(hdy, non_blocking=True)
+            L.forward(dx_in)
+            L.backward(dx_in, dy_in, accumulate=True)
+            hy.copy_(L.y, non_blocking=True)
+            hdx.copy_(L.dx, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(a.elapsed_time(b), world)
+        es = x.element_size()
+        e2e = {"value": world * s.T * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": (x.numel() + dy.numel()) * es,
+               "d2h_bytes_per_step": (L.y.numel() + L.dx.numel()) * es,
+               "note": "pinned host x, dy -> device; forward + backward; y, dx -> pinned host; no L2 flush"}
+
+    if rank != 0:
+        return
+    work = algorithmic_work(s, N)
+    hbm, tflops, peak_kind = peaks()
+    kernels = {}
+    for name, (n, ms) in prof.items():
+        avg = ms / n
+        entry = {"launches": n, "total_ms": round(ms, 4), "avg_us": round(1e3 * avg, 2),
+                 "share": round(ms / sum(v[1] for v in prof.values()), 4)}
+        if name in work:
+            unit, amount = work[name]
+            if unit == "flops":
+                entry["tflops"] = round(amount / (avg / 1e3) / 1e12, 1)
+                entry["frac_of_bf16_peak"] = round(amount / (avg / 1e3) / 1e12 / tflops, 3)
+            else:
+                entry["gbs"] = round(amount / (avg / 1e3) / 1e9, 1)
+                entry["frac_of_hbm"] = round(amount / (avg / 1e3) / 1e9 / hbm, 3)
+        kernels[name] = entry
+    dom = max(prof.items(), key=lambda kv: kv[1][1])[0]
+    unit, amount = work.get(dom, ("flops", 0))
+    avg_s = prof[dom][1] / prof[dom][0] / 1e3
+    if unit == "flops":
+        achieved = amount / avg_s / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": tflops, "unit": "TFLOP/s",
+                "frac": round(achieved / tflops, 4)}
+    else:
+        achieved = amount / avg_s / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4)}
+    roof["kernel"] = dom
+    roof["traffic"] = committed_traffic(dom)
+    roof["peak_source"] = f"{peak_kind} ({'bf16_tflops_sustained' if unit == 'flops' else 'hbm_gbs'})"
+    gemm_names = [n for n in kernels if n.startswith("gemm_")]
+    gemm_flops = sum(work[n][1] * prof[n][0] for n in gemm_names)
+    gemm_ms = sum(prof[n][1] for n in gemm_names)
+    value = world * s.T * args.steps / (total_ms / 1e3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": s.dtype, "data": "synthetic",
+        "config": {"workload": args.workload, "T": s.T, "d_model": s.d_model, "d_ff": s.d_ff, "E": s.E, "k": s.k,
+                   "capacity_factor": s.capacity_factor, "kept_assignments": N,
+                   "step": "forward + backward (fp32 grad accumulate)",
+                   "l2": "256 MB buffer written before every timed step, outside the step's events",
+                   "parallelism": f"replicas x{world}"},
+        "fwd_tokens_per_s": world * s.T * args.steps / (fwd_ms / 1e3),
+        "grouped_gemm_frac_bf16_peak": round(gemm_flops / (gemm_ms / 1e3) / 1e12 / tflops, 4) if gemm_ms else None,
+        "permute_gbs": kernels.get("permute", {}).get("gbs"),
+        "roofline": roof,
+        "gpu_launches": launches,
+        "clocks": clk,
+        "kernels": kernels,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline:
+        try:
+            line["cpu_baseline"] = cpu_baseline(args.workload, s.T, args.cpu_seconds)
+        except Exception as exc:  # report, do not hide, a failed baseline
+            line["cpu_baseline"] = {"value": None, "error": str(exc)[-300:]}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_init(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

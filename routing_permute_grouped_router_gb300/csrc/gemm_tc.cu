@@ -1,0 +1,717 @@
+// bf16 grouped GEMMs of the expert FFN on the 5th-generation tensor cores.
+//
+// The permute makes each expert's tokens one contiguous row segment, so the
+// expert computation is one grouped matrix multiply over ragged segments
+// ("The permutation step matters more than it looks", gpu_expert_parallel
+// page).  Five products share one persistent kernel:
+//
+//   UP      [a | b] = X_e [W1_e | W3_e]   -> h = silu(a) * b (and a, b)   A K-major, B MN-major
+//   DOWN    y_perm  = H_e W2_e                                            A K-major, B MN-major
+//   DGRAD_H dH = dY_e W2_e^T -> da, db (SwiGLU backward in the epilogue)  A K-major, B K-major
+//   DGRAD_X dx_perm = [da | db] [W1_e | W3_e]^T (K concatenated)          A K-major, B K-major
+//   WGRAD   dW1_e = X_e^T da, dW3_e = X_e^T db, dW2_e = H_e^T dY_e (fp32)  A MN-major, B MN-major
+//
+// Structure (one CTA per SM, 192 threads):
+//   warp 0, one lane: TMA producer; 128x64 A and 256x64 B bf16 tiles in
+//     128-byte-swizzled shared memory, 4-stage mbarrier ring;
+//   warp 1: allocates 512 TMEM columns; one lane issues tcgen05.mma
+//     (M=128, N=256, K=16, fp32 accumulate) into one of two 256-column
+//     accumulators and commits stage releases and accumulator-ready events;
+//   warps 2-5: epilogue; tcgen05.ld moves a 32-row x 32-column slice per
+//     warp into registers, the fused math runs there, results go to HBM.
+// Tiles are taken round-robin from a list the kernel derives on the device
+// from offsets/counts, so the host never reads the routing outcome.  Every
+// mbarrier wait is bounded (2 s); on expiry the kernel records
+// DEV_TIMEOUT in the error word, drains its own copies and MMAs, frees TMEM
+// and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int NSTAGE = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int CTRL_BYTES = 2048;
+constexpr int SMEM_BYTES = NSTAGE * STAGE_BYTES + CTRL_BYTES + 1024;  // + alignment slack
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+constexpr int MAX_E = 128;
+
+enum Mode { M_UP = 0, M_DOWN = 1, M_DGRAD_H = 2, M_DGRAD_X = 3, M_WGRAD = 4 };
+
+struct TcMaps {
+  CUtensorMap m[6];
+};
+
+struct TcArgs {
+  const int32_t* counts;
+  const int32_t* offsets;
+  int E, d, f;
+  int64_t max_rows;
+  __nv_bfloat16* o0;  // UP: h      DOWN: y_perm   DGRAD_H: da   DGRAD_X: dx_perm
+  __nv_bfloat16* o1;  // UP: a (or null)           DGRAD_H: db
+  __nv_bfloat16* o2;  // UP: b (or null)
+  const __nv_bfloat16* i0;  // DGRAD_H: a
+  const __nv_bfloat16* i1;  // DGRAD_H: b
+  float* w0;  // WGRAD: dW1
+  float* w1;  // WGRAD: dW3
+  float* w2;  // WGRAD: dW2
+  int accumulate;
+  uint32_t* err;
+};
+
+// ------------------------------ PTX wrappers ------------------------------ //
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for the phase of `parity` to complete.  Gives up after WAIT_LIMIT_NS or
+// when another role has raised the abort flag; returns false then.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t* err,
+                                       uint32_t where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1; i < (1u << 30); ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > WAIT_LIMIT_NS) break;
+    }
+  }
+  *abort_flag = 1;
+  report_error(err, DEV_TIMEOUT, where);
+  return false;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], "
+      "[%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+// Waits for this thread's tcgen05.ld and ties the loaded registers to the wait,
+// so no use of them can be scheduled ahead of it.
+#define TMEM_REGS32(r)                                                                                    \
+  "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),          \
+      "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), \
+      "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]),           \
+      "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),           \
+      "+r"(r[30]), "+r"(r[31])
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : TMEM_REGS32(r)::"memory");
+}
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) { asm volatile("" : TMEM_REGS32(r)::"memory"); }
+
+// Shared-memory matrix descriptor, 128-byte swizzle, sm_100 family version bit.
+//   K-major tile: rows of 64 bf16 (128 B), 8-row atoms 1024 B apart (SBO).
+//   MN-major tile: 64 MN-contiguous bf16 per 128-B row, one row per K;
+//     8-K-row atoms 1024 B apart (SBO), 64-wide MN chunks 8 KB apart (LBO).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+// Instruction descriptor of kind::f16: fp32 D, bf16 A and B, M = 128, N = 256.
+__host__ __device__ constexpr uint32_t idesc_bf16(bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.f + __expf(-z)); }
+
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&v)[32]) {
+  uint4* p = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    float w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = v[8 * q + i];
+    p[q] = pack(w);
+  }
+}
+__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float (&v)[32]) {
+  const uint4* p = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    float w[8];
+    unpack(__ldg(p + q), w);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[8 * q + i] = w[i];
+  }
+}
+
+// ------------------------------ tile schedule ------------------------------ //
+struct Tile {
+  int e;
+  int64_t row0;  // first row of the tile (ragged-M modes) / first K row (WGRAD)
+  int m0, n0;    // WGRAD: output tile origin; other modes: n0 only
+  int sub;       // WGRAD product: 0 = dW1, 1 = dW3, 2 = dW2
+  int kblocks;
+};
+
+template <int MODE>
+__device__ __forceinline__ int n_tiles_of(const TcArgs& a) {
+  if (MODE == M_UP) return a.f / 128;
+  if (MODE == M_DOWN || MODE == M_DGRAD_X) return a.d / BN;
+  return a.f / BN;  // DGRAD_H
+}
+
+template <int MODE>
+__device__ __forceinline__ Tile decode(int tile, const TcArgs& a, const int* s_off, const int* s_cnt) {
+  Tile t{};
+  if (MODE == M_WGRAD) {
+    const int P = (a.d / BM) * (a.f / BN);
+    t.e = tile / (3 * P);
+    const int q = tile % (3 * P);
+    if (q < 2 * P) {
+      t.sub = q & 1;
+      const int r = q >> 1, nt = a.f / BN;
+      t.m0 = (r / nt) * BM;
+      t.n0 = (r % nt) * BN;
+    } else {
+      t.sub = 2;
+      const int r = q - 2 * P, nt = a.d / BN;
+      t.m0 = (r / nt) * BM;
+      t.n0 = (r % nt) * BN;
+    }
+    t.row0 = s_off[t.e];
+    t.kblocks = (s_cnt[t.e] + BK - 1) / BK;
+  } else {
+    const int nt = n_tiles_of<MODE>(a);
+    const int mt = tile / nt;
+    t.n0 = (tile % nt) * (MODE == M_UP ? 128 : BN);
+    t.row0 = (int64_t)mt * BM;
+    int lo = 0, hi = a.E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_off[mid] <= t.row0) lo = mid;
+      else hi = mid - 1;
+    }
+    t.e = lo;
+    const int K = (MODE == M_UP || MODE == M_DGRAD_H) ? a.d : (MODE == M_DOWN ? a.f : 2 * a.f);
+    t.kblocks = K / BK;
+  }
+  return t;
+}
+
+template <int MODE>
+__device__ __forceinline__ void issue_stage(const TcMaps& maps, const TcArgs& a, const Tile& t, int kb, uint32_t sA,
+                                            uint32_t sB, uint32_t bar) {
+  const int r0 = static_cast<int>(t.row0);
+  if (MODE == M_UP) {
+    tma_load_2d(sA, &maps.m[0], bar, kb * BK, r0);
+    const int wr = t.e * a.d + kb * BK;
+    tma_load_2d(sB + 0 * 8192, &maps.m[1], bar, t.n0, wr);
+    tma_load_2d(sB + 1 * 8192, &maps.m[1], bar, t.n0 + 64, wr);
+    tma_load_2d(sB + 2 * 8192, &maps.m[2], bar, t.n0, wr);
+    tma_load_2d(sB + 3 * 8192, &maps.m[2], bar, t.n0 + 64, wr);
+  } else if (MODE == M_DOWN) {
+    tma_load_2d(sA, &maps.m[0], bar, kb * BK, r0);
+    const int wr = t.e * a.f + kb * BK;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tma_load_2d(sB + c * 8192, &maps.m[1], bar, t.n0 + 64 * c, wr);
+  } else if (MODE == M_DGRAD_H) {
+    tma_load_2d(sA, &maps.m[0], bar, kb * BK, r0);
+    tma_load_2d(sB, &maps.m[1], bar, kb * BK, t.e * a.f + t.n0);
+  } else if (MODE == M_DGRAD_X) {
+    const int kf = a.f / BK;
+    if (kb < kf) {
+      tma_load_2d(sA, &maps.m[0], bar, kb * BK, r0);
+      tma_load_2d(sB, &maps.m[2], bar, kb * BK, t.e * a.d + t.n0);
+    } else {
+      tma_load_2d(sA, &maps.m[1], bar, (kb - kf) * BK, r0);
+      tma_load_2d(sB, &maps.m[3], bar, (kb - kf) * BK, t.e * a.d + t.n0);
+    }
+  } else {  // WGRAD
+    const CUtensorMap* am = t.sub == 2 ? &maps.m[1] : &maps.m[0];
+    const CUtensorMap* bm = t.sub == 0 ? &maps.m[2] : (t.sub == 1 ? &maps.m[3] : &maps.m[4]);
+    const int kr = r0 + kb * BK;
+    tma_load_2d(sA, am, bar, t.m0, kr);
+    tma_load_2d(sA + 8192, am, bar, t.m0 + 64, kr);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tma_load_2d(sB + c * 8192, bm, bar, t.n0 + 64 * c, kr);
+  }
+}
+
+// ------------------------------ epilogues --------------------------------- //
+template <int MODE>
+__device__ __forceinline__ void epilogue_tile(const TcArgs& a, const Tile& t, uint32_t tacc, int q, int lane) {
+  const int64_t row = t.row0 + q * 32 + lane;
+  if (MODE == M_UP) {
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t ra[32], rb[32];
+      tmem_ld32(tacc + c * 32, ra);
+      tmem_ld32(tacc + 128 + c * 32, rb);
+      tmem_ld_wait(ra);
+      reg_fence(rb);
+      float hv[32], av[32], bv[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        av[i] = __uint_as_float(ra[i]);
+        bv[i] = __uint_as_float(rb[i]);
+        hv[i] = silu_f(av[i]) * bv[i];
+      }
+      const int64_t o = row * a.f + t.n0 + c * 32;
+      store_bf16x32(a.o0 + o, hv);
+      if (a.o1 != nullptr) store_bf16x32(a.o1 + o, av);
+      if (a.o2 != nullptr) store_bf16x32(a.o2 + o, bv);
+    }
+  } else if (MODE == M_DOWN || MODE == M_DGRAD_X) {
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+      uint32_t r[32];
+      tmem_ld32(tacc + c * 32, r);
+      tmem_ld_wait(r);
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+      store_bf16x32(a.o0 + row * a.d + t.n0 + c * 32, v);
+    }
+  } else if (MODE == M_DGRAD_H) {
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+      uint32_t r[32];
+      tmem_ld32(tacc + c * 32, r);
+      const int64_t o = row * a.f + t.n0 + c * 32;
+      float av[32], bv[32];
+      load_bf16x32(a.i0 + o, av);
+      load_bf16x32(a.i1 + o, bv);
+      tmem_ld_wait(r);
+      float dav[32], dbv[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float dh = __uint_as_float(r[i]);
+        const float s = 1.f / (1.f + __expf(-av[i]));
+        dav[i] = dh * bv[i] * s * (1.f + av[i] * (1.f - s));
+        dbv[i] = dh * av[i] * s;
+      }
+      store_bf16x32(a.o0 + o, dav);
+      store_bf16x32(a.o1 + o, dbv);
+    }
+  } else {  // WGRAD: fp32 rows of the weight gradient
+    const int M = t.sub == 2 ? a.f : a.d, N = t.sub == 2 ? a.d : a.f;
+    float* out = t.sub == 0 ? a.w0 : (t.sub == 1 ? a.w1 : a.w2);
+    float* dst = out + ((int64_t)t.e * M + t.m0 + q * 32 + lane) * N + t.n0;
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+      float v[32];
+      if (t.kblocks > 0) {
+        uint32_t r[32];
+        tmem_ld32(tacc + c * 32, r);
+        tmem_ld_wait(r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+      } else {
+        if (a.accumulate) continue;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+      }
+      float4* p = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float4 w = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        if (a.accumulate) {
+          const float4 old = p[i];
+          w.x += old.x;
+          w.y += old.y;
+          w.z += old.z;
+          w.w += old.w;
+        }
+        p[i] = w;
+      }
+    }
+  }
+}
+
+// ------------------------------ the kernel -------------------------------- //
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcMaps maps,
+                                                             const __grid_constant__ TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ctrl = smem + NSTAGE * STAGE_BYTES;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(ctrl);
+  uint64_t* empty_bar = full_bar + NSTAGE;
+  uint64_t* tfull_bar = empty_bar + NSTAGE;
+  uint64_t* tempty_bar = tfull_bar + 2;
+  uint64_t* drain_bar = tempty_bar + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* s_total = reinterpret_cast<int*>(tmem_slot + 2);
+  int* s_off = reinterpret_cast<int*>(ctrl + 128);        // E + 1 ints
+  int* s_cnt = s_off + MAX_E + 1;                         // E ints
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NSTAGE; ++i) {
+      mbar_init(smem_addr(&full_bar[i]), 1);
+      mbar_init(smem_addr(&empty_bar[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_addr(&tfull_bar[i]), 1);
+      mbar_init(smem_addr(&tempty_bar[i]), 4);
+    }
+    mbar_init(smem_addr(drain_bar), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  for (int i = threadIdx.x; i <= a.E; i += THREADS) s_off[i] = a.offsets[i];
+  for (int i = threadIdx.x; i < a.E; i += THREADS) s_cnt[i] = a.counts[i];
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x == 0) {
+    // validate the routing state before trusting it for addresses
+    bool ok = s_off[0] == 0 && (int64_t)s_off[a.E] <= a.max_rows;
+    for (int e = 0; e < a.E && ok; ++e) {
+      const int len = s_off[e + 1] - s_off[e];
+      ok = len >= 0 && (s_off[e] & (BM - 1)) == 0 && s_cnt[e] >= 0 && s_cnt[e] <= len;
+    }
+    ok = ok && (s_off[a.E] & (BM - 1)) == 0;
+    int total = 0;
+    if (ok) {
+      if (MODE == M_WGRAD) total = a.E * 3 * (a.d / BM) * (a.f / BN);
+      else total = (s_off[a.E] / BM) * n_tiles_of<MODE>(a);
+    } else if (blockIdx.x == 0) {
+      report_error(a.err, DEV_BAD_OFFSETS, 30 + MODE);
+    }
+    *s_total = total;
+  }
+  __syncthreads();
+  const int total = *s_total;
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t smem_base = smem_addr(smem);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      constexpr int NMAPS = MODE == M_UP ? 3 : (MODE == M_DGRAD_X ? 4 : (MODE == M_WGRAD ? 5 : 2));
+      for (int i = 0; i < NMAPS; ++i) prefetch_map(&maps.m[i]);
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool alive = true;
+      for (int tile = blockIdx.x; tile < total && alive; tile += gridDim.x) {
+        const Tile t = decode<MODE>(tile, a, s_off, s_cnt);
+        for (int kb = 0; kb < t.kblocks; ++kb) {
+          if (!mbar_wait(smem_addr(&empty_bar[stage]), phase ^ 1u, abort_flag, a.err, 100 + MODE)) {
+            alive = false;
+            break;
+          }
+          const uint32_t fb = smem_addr(&full_bar[stage]);
+          mbar_expect_tx(fb, STAGE_BYTES);
+          const uint32_t sA = smem_base + stage * STAGE_BYTES;
+          issue_stage<MODE>(maps, a, t, kb, sA, sA + A_BYTES, fb);
+          ++issued;
+          if (++stage == NSTAGE) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!alive) {
+        // drain the copies still in flight before the CTA may exit
+        int n = issued < NSTAGE ? issued : NSTAGE;
+        int s = stage;
+        uint32_t ph = phase;
+        for (int i = 0; i < n; ++i) {
+          if (--s < 0) {
+            s = NSTAGE - 1;
+            ph ^= 1u;
+          }
+          const uint32_t fb = smem_addr(&full_bar[s]);
+          for (uint32_t it = 0; it < (1u << 24) && !mbar_try_wait(fb, ph); ++it) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      constexpr bool A_MN = MODE == M_WGRAD;
+      constexpr bool B_MN = MODE == M_UP || MODE == M_DOWN || MODE == M_WGRAD;
+      constexpr uint32_t IDESC = idesc_bf16(A_MN, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool alive = true;
+      for (int tile = blockIdx.x; tile < total && alive; tile += gridDim.x, ++local) {
+        const Tile t = decode<MODE>(tile, a, s_off, s_cnt);
+        const int acc = local & 1;
+        const uint32_t use = (uint32_t)(local >> 1) & 1u;
+        if (!mbar_wait(smem_addr(&tempty_bar[acc]), use ^ 1u, abort_flag, a.err, 200 + MODE)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < t.kblocks; ++kb) {
+          if (!mbar_wait(smem_addr(&full_bar[stage]), phase, abort_flag, a.err, 300 + MODE)) {
+            alive = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sA = smem_base + stage * STAGE_BYTES;
+          const uint32_t sB = sA + A_BYTES;
+#pragma unroll
+          for (int k16 = 0; k16 < BK / 16; ++k16) {
+            const uint64_t ad = A_MN ? sdesc(sA + k16 * 2048, 8192, 1024) : sdesc(sA + k16 * 32, 16, 1024);
+            const uint64_t bd = B_MN ? sdesc(sB + k16 * 2048, 8192, 1024) : sdesc(sB + k16 * 32, 16, 1024);
+            umma_bf16(d_tmem, ad, bd, IDESC, (kb | k16) != 0 ? 1u : 0u);
+          }
+          umma_commit(smem_addr(&empty_bar[stage]));
+          if (++stage == NSTAGE) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!alive) break;
+        umma_commit(smem_addr(&tfull_bar[acc]));
+      }
+      // all MMAs of this thread complete before TMEM can be released
+      umma_commit(smem_addr(drain_bar));
+      for (uint32_t it = 0; it < (1u << 26) && !mbar_try_wait(smem_addr(drain_bar), 0); ++it) {
+      }
+    }
+  } else {
+    // ---------------- epilogue warps 2..5 ----------------
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int local = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
+      const Tile t = decode<MODE>(tile, a, s_off, s_cnt);
+      const int acc = local & 1;
+      const uint32_t use = (uint32_t)(local >> 1) & 1u;
+      if (!mbar_wait(smem_addr(&tfull_bar[acc]), use, abort_flag, a.err, 400 + MODE)) break;
+      tc_fence_after();
+      const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+      epilogue_tile<MODE>(a, t, tacc, q, lane);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&tempty_bar[acc]));
+    }
+  }
+  __syncwarp();
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// ------------------------------ host side --------------------------------- //
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+bool g_encode_tried = false;
+
+bool resolve_encode() {
+  if (!g_encode_tried) {
+    g_encode_tried = true;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return g_encode != nullptr;
+}
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+              uint32_t box_rows) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 1;
+  }
+  return cached[dev];
+}
+
+template <int MODE>
+cudaError_t launch_mode(const TcMaps& maps, const TcArgs& args, int64_t tile_bound, int kind, cudaStream_t st) {
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!attr_done[dev]) {
+    cudaError_t e =
+        cudaFuncSetAttribute(tc_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  if (tile_bound <= 0) return cudaSuccess;
+  const int grid = (int)(tile_bound < num_sms() ? tile_bound : num_sms());
+  LaunchScope ls(kind, st);
+  tc_gemm_kernel<MODE><<<grid, THREADS, SMEM_BYTES, st>>>(maps, args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_driver_ready() { return resolve_encode(); }
+
+cudaError_t tc_ffn_fwd(const Shape& s, const FfnFwdArgs& f, uint32_t* err, cudaStream_t st) {
+  if (!resolve_encode()) return cudaErrorNotSupported;
+  if (s.max_rows == 0) return cudaSuccess;
+  const uint64_t R = (uint64_t)s.max_rows, E = (uint64_t)s.E, d = (uint64_t)s.d, ff = (uint64_t)s.f;
+  TcArgs a{};
+  a.counts = f.counts;
+  a.offsets = f.offsets;
+  a.E = s.E;
+  a.d = s.d;
+  a.f = s.f;
+  a.max_rows = s.max_rows;
+  a.err = err;
+  TcMaps up{}, down{};
+  bool ok = make_map(&up.m[0], f.x_perm, R, d, 64, BM) && make_map(&up.m[1], f.W1, E * d, ff, 64, 64) &&
+            make_map(&up.m[2], f.W3, E * d, ff, 64, 64);
+  ok = ok && make_map(&down.m[0], f.h, R, ff, 64, BM) && make_map(&down.m[1], f.W2, E * ff, d, 64, 64);
+  if (!ok) return cudaErrorInvalidValue;
+  const int64_t mt = s.max_rows / BM;
+  a.o0 = static_cast<__nv_bfloat16*>(f.h);
+  a.o1 = static_cast<__nv_bfloat16*>(f.a);
+  a.o2 = static_cast<__nv_bfloat16*>(f.b);
+  cudaError_t e = launch_mode<M_UP>(up, a, mt * (s.f / 128), KK_GEMM_UP, st);
+  if (e != cudaSuccess) return e;
+  a.o0 = static_cast<__nv_bfloat16*>(f.y_perm);
+  a.o1 = a.o2 = nullptr;
+  return launch_mode<M_DOWN>(down, a, mt * (s.d / BN), KK_GEMM_DOWN, st);
+}
+
+cudaError_t tc_ffn_bwd(const Shape& s, const FfnBwdArgs& b, uint32_t* err, cudaStream_t st) {
+  if (!resolve_encode()) return cudaErrorNotSupported;
+  const uint64_t E = (uint64_t)s.E, d = (uint64_t)s.d, ff = (uint64_t)s.f;
+  if (s.max_rows == 0) {
+    if (b.accumulate) return cudaSuccess;
+    cudaError_t e = cudaMemsetAsync(b.dW1, 0, E * d * ff * 4, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(b.dW3, 0, E * d * ff * 4, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(b.dW2, 0, E * d * ff * 4, st);
+    return e;
+  }
+  const uint64_t R = (uint64_t)s.max_rows;
+  TcArgs a{};
+  a.counts = b.counts;
+  a.offsets = b.offsets;
+  a.E = s.E;
+  a.d = s.d;
+  a.f = s.f;
+  a.max_rows = s.max_rows;
+  a.err = err;
+  a.accumulate = b.accumulate;
+  TcMaps mh{}, mw{}, mx{};
+  bool ok = make_map(&mh.m[0], b.dy_perm, R, d, 64, BM) && make_map(&mh.m[1], b.W2, E * ff, d, 64, BN);
+  ok = ok && make_map(&mw.m[0], b.x_perm, R, d, 64, 64) && make_map(&mw.m[1], b.h, R, ff, 64, 64) &&
+       make_map(&mw.m[2], b.da, R, ff, 64, 64) && make_map(&mw.m[3], b.db, R, ff, 64, 64) &&
+       make_map(&mw.m[4], b.dy_perm, R, d, 64, 64);
+  ok = ok && make_map(&mx.m[0], b.da, R, ff, 64, BM) && make_map(&mx.m[1], b.db, R, ff, 64, BM) &&
+       make_map(&mx.m[2], b.W1, E * d, ff, 64, BN) && make_map(&mx.m[3], b.W3, E * d, ff, 64, BN);
+  if (!ok) return cudaErrorInvalidValue;
+  const int64_t mt = s.max_rows / BM;
+  a.o0 = static_cast<__nv_bfloat16*>(b.da);
+  a.o1 = static_cast<__nv_bfloat16*>(b.db);
+  a.i0 = static_cast<const __nv_bfloat16*>(b.a);
+  a.i1 = static_cast<const __nv_bfloat16*>(b.b);
+  cudaError_t e = launch_mode<M_DGRAD_H>(mh, a, mt * (s.f / BN), KK_GEMM_DGRAD_H, st);
+  if (e != cudaSuccess) return e;
+  a.w0 = b.dW1;
+  a.w1 = b.dW3;
+  a.w2 = b.dW2;
+  e = launch_mode<M_WGRAD>(mw, a, (int64_t)s.E * 3 * (s.d / BM) * (s.f / BN), KK_GEMM_WGRAD, st);
+  if (e != cudaSuccess) return e;
+  a.o0 = static_cast<__nv_bfloat16*>(b.dx_perm);
+  a.o1 = nullptr;
+  return launch_mode<M_DGRAD_X>(mx, a, mt * (s.d / BN), KK_GEMM_DGRAD_X, st);
+}
+
+}  // namespace moe

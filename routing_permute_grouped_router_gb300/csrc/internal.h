@@ -1,0 +1,107 @@
+// Internal declarations shared by the library's translation units: kernel
+// kinds for launch accounting, the device error word codes, and the launchers
+// that the C ABI layer (moe_api.cu) sequences.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+enum KernelKind : int {
+  KK_ROUTER = 0,
+  KK_SLOT_SCAN,
+  KK_SLOT_ASSIGN,
+  KK_PERMUTE,
+  KK_GEMM_UP,
+  KK_GEMM_DOWN,
+  KK_COMBINE,
+  KK_COMBINE_BWD,
+  KK_GEMM_DGRAD_H,
+  KK_GEMM_WGRAD,
+  KK_GEMM_DGRAD_X,
+  KK_TRANSPOSE_WR,
+  KK_DX_ROUTER,
+  KK_DWR_PARTIAL,
+  KK_DWR_REDUCE,
+  KK_ZERO,
+  KK_COUNT
+};
+
+// Device error word: err[0] = first code (0 = none), err[1] = detail of that code.
+enum DevErr : uint32_t {
+  DEV_OK = 0,
+  DEV_BAD_ROW = 1,      // a row index outside [0, max_rows)
+  DEV_BAD_EXPERT = 2,   // an expert id outside [0, E)
+  DEV_BAD_OFFSETS = 3,  // offsets not monotone / not 128-aligned / beyond max_rows
+  DEV_TIMEOUT = 4,      // a pipeline wait ran out of time
+  DEV_BAD_COUNT = 5     // counts[e] larger than its segment
+};
+
+// Launch accounting (defined in moe_api.cu): every kernel launch is bracketed
+// by launch_begin/launch_end so the library can count launches and, when the
+// profiler is on, record CUDA events around it on the launch stream.
+void launch_begin(int kind, cudaStream_t s);
+void launch_end(int kind, cudaStream_t s);
+
+struct LaunchScope {
+  int kind;
+  cudaStream_t s;
+  LaunchScope(int k, cudaStream_t st) : kind(k), s(st) { launch_begin(kind, s); }
+  ~LaunchScope() { launch_end(kind, s); }
+};
+
+struct Shape {
+  int T, d, f, E, k;
+  int cap;           // INT32_MAX when dropless
+  int bf16;          // 1 = bf16 activations/weights, 0 = fp32
+  int64_t max_rows;  // bound on offsets[E]
+};
+
+// ---- routing.cu ----
+// Router GEMV/top-k, then the per-expert scan, then slot assignment.
+cudaError_t launch_router(const Shape& s, const void* x, const float* W_r, const float* bias, int32_t* ids,
+                          float* gates, float* probs, int32_t* hist, int32_t* ticket, cudaStream_t st);
+cudaError_t launch_slot_scan(const Shape& s, const int32_t* hist, int32_t* base, int32_t* totals,
+                             int32_t* ticket, int32_t* counts, int32_t* offsets, uint32_t* err, cudaStream_t st);
+cudaError_t launch_slot_assign(const Shape& s, const int32_t* ids, const int32_t* base, const int32_t* counts,
+                               const int32_t* offsets, int32_t* slot, int32_t* row_of, int32_t* src_token,
+                               uint32_t* err, cudaStream_t st);
+int router_blocks(int T);  // tokens per router block is fixed; this is the block count
+
+// ---- rows.cu ----
+cudaError_t launch_permute(const Shape& s, const void* x, const int32_t* row_of, const int32_t* counts,
+                           const int32_t* offsets, void* x_perm, uint32_t* err, cudaStream_t st);
+cudaError_t launch_combine(const Shape& s, const void* y_perm, const int32_t* row_of, const float* gates, void* y,
+                           uint32_t* err, cudaStream_t st);
+cudaError_t launch_combine_bwd(const Shape& s, const void* dy, const void* y_perm, const int32_t* ids,
+                               const int32_t* row_of, const float* gates, const float* probs,
+                               const int32_t* counts, const int32_t* offsets, void* dy_perm, float* dg, float* dl,
+                               uint32_t* err, cudaStream_t st);
+cudaError_t launch_dx_router(const Shape& s, const void* dx_perm, const int32_t* row_of, const float* dl,
+                             const float* W_r, float* W_rT, void* dx, uint32_t* err, cudaStream_t st);
+cudaError_t launch_dwr(const Shape& s, const void* x, const float* dl, float* partial, int splits, float* dW_r,
+                       int accumulate, cudaStream_t st);
+int dwr_splits(const Shape& s);
+cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t st);
+
+// ---- gemm_tc.cu (bf16, tcgen05) and gemm_simt.cu (fp32) ----
+struct FfnFwdArgs {
+  const void* x_perm; const int32_t* counts; const int32_t* offsets;
+  const void* W1; const void* W3; const void* W2;
+  void* h; void* y_perm; void* a; void* b;
+};
+struct FfnBwdArgs {
+  const void* x_perm; const void* a; const void* b; const void* h; const void* dy_perm;
+  const int32_t* counts; const int32_t* offsets;
+  const void* W1; const void* W3; const void* W2;
+  void* da; void* db; void* dx_perm;
+  float* dW1; float* dW3; float* dW2; int accumulate;
+};
+cudaError_t tc_ffn_fwd(const Shape& s, const FfnFwdArgs& a, uint32_t* err, cudaStream_t st);
+cudaError_t tc_ffn_bwd(const Shape& s, const FfnBwdArgs& a, uint32_t* err, cudaStream_t st);
+cudaError_t simt_ffn_fwd(const Shape& s, const FfnFwdArgs& a, uint32_t* err, cudaStream_t st);
+cudaError_t simt_ffn_bwd(const Shape& s, const FfnBwdArgs& a, uint32_t* err, cudaStream_t st);
+bool tc_driver_ready();  // tensor-map encoder resolved from the driver
+
+}  // namespace moe
