@@ -331,3 +331,93 @@ def train_step(xs, dys, W_r, bias, W1, W3, W2, k: int, C: Optional[int]) -> Dict
             for n in acc:
                 acc[n] += gr[n]
     return dict(grads=acc, micro_batches=outs)
+
+
+# --------------------------------------------------------------------------- #
+# Exact outputs at full size, one token or a few weight columns at a time.
+# The same formulas as above restricted to a subset, for layers too large to
+# run whole on the CPU.
+# --------------------------------------------------------------------------- #
+def token_outputs(t: int, x, dy, W_r, bias, W1, W3, W2, st, want_dx: bool = True) -> Dict[str, np.ndarray]:
+    """y[t] and (optionally) dx[t] of token t from the routing state ``st`` of its batch.
+
+    ``st`` needs ids, gates, probs and slot (from ``route`` on the full batch);
+    a token's output depends only on its own row, its picks and whether each
+    pick was kept.
+    """
+    xt = np.asarray(x[t], np.float64)
+    k = st["ids"].shape[1]
+    Ys, dX = [], np.zeros_like(xt)
+    y = np.zeros_like(xt)
+    for j in range(k):
+        e = int(st["ids"][t, j])
+        if st["slot"][t, j] < 0:
+            Ys.append(None)
+            continue
+        a, b, h, Y = expert_ffn(xt[None, :], np.asarray(W1[e], np.float64), np.asarray(W3[e], np.float64),
+                                np.asarray(W2[e], np.float64))
+        Ys.append((a[0], b[0], Y[0]))
+        y += st["gates"][t, j] * Y[0]
+    out = dict(y=y)
+    if not want_dx:
+        return out
+    dyt = np.asarray(dy[t], np.float64)
+    dg = np.array([[0.0 if Ys[j] is None else float(np.dot(dyt, Ys[j][2])) for j in range(k)]])
+    one = {n: st[n][t:t + 1] for n in ("ids", "gates", "probs")}
+    dl = router_logit_grad(dg, one)[0]
+    for j in range(k):
+        if Ys[j] is None:
+            continue
+        e = int(st["ids"][t, j])
+        a, b, _ = Ys[j]
+        dY = st["gates"][t, j] * dyt
+        dH = np.asarray(W2[e], np.float64) @ dY
+        s = sigmoid(a)
+        da = dH * b * s * (1.0 + a * (1.0 - s))
+        db = dH * silu(a)
+        dX += np.asarray(W1[e], np.float64) @ da + np.asarray(W3[e], np.float64) @ db
+    out["dx"] = dX + np.asarray(W_r, np.float64) @ dl
+    out["dl"] = dl
+    out["dg"] = dg[0]
+    return out
+
+
+def weight_grad_columns(x, dy, W1, W3, W2, st, cols) -> Dict[str, np.ndarray]:
+    """dW1[:, :, cols], dW3[:, :, cols] and dW2[:, cols, :] of one micro-batch.
+
+    Column j of a, b, h, dH, da, db depends only on column j of W1, W3 and row j
+    of W2, so the expert backward restricted to ``cols`` is exact.
+    """
+    cols = np.asarray(cols)
+    E = W1.shape[0]
+    d = W1.shape[1]
+    out = dict(dW1=np.zeros((E, d, cols.size)), dW3=np.zeros((E, d, cols.size)),
+               dW2=np.zeros((E, cols.size, W2.shape[2])))
+    x = np.asarray(x, np.float64)
+    dy = np.asarray(dy, np.float64)
+    T, k = st["ids"].shape
+    for e in range(E):
+        toks, gs = [], []
+        for j in range(k):
+            for t in range(T):
+                if st["ids"][t, j] == e and st["slot"][t, j] >= 0:
+                    toks.append(t)
+                    gs.append(st["gates"][t, j])
+        if not toks:
+            continue
+        X = x[toks]
+        dY = np.asarray(gs)[:, None] * dy[toks]
+        W1c = np.asarray(W1[e][:, cols], np.float64)
+        W3c = np.asarray(W3[e][:, cols], np.float64)
+        W2r = np.asarray(W2[e][cols, :], np.float64)
+        a = X @ W1c
+        b = X @ W3c
+        h = silu(a) * b
+        dH = dY @ W2r.T
+        s = sigmoid(a)
+        da = dH * b * s * (1.0 + a * (1.0 - s))
+        db = dH * silu(a)
+        out["dW1"][e] = X.T @ da
+        out["dW3"][e] = X.T @ db
+        out["dW2"][e] = h.T @ dY
+    return out

@@ -345,3 +345,23 @@ def test_planted_mistake_is_caught(monkeypatch, mutation):
             return s, c
         monkeypatch.setattr(O, "assign_slots", bad)
     assert not _pins_pass(), mutation
+
+
+def test_token_and_column_helpers_agree_with_the_whole_layer():
+    rng = np.random.default_rng(21)
+    T, d, f, E, k = 40, 6, 9, 5, 2
+    x, W_r, W1, W3, W2 = _rand_layer(rng, T, d, f, E)
+    dy = rng.standard_normal((T, d))
+    st = O.forward(x, W_r, None, W1, W3, W2, k, 9)
+    gr = O.backward(dy, x, W_r, W1, W3, W2, st)
+    assert (st["slot"] < 0).any()
+    for t in (0, 7, 39):
+        o = O.token_outputs(t, x, dy, W_r, None, W1, W3, W2, st)
+        np.testing.assert_allclose(o["y"], st["y"][t], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(o["dx"], gr["dx"][t], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(o["dl"], gr["dl"][t], rtol=1e-12, atol=1e-12)
+    cols = [0, 4, 8]
+    c = O.weight_grad_columns(x, dy, W1, W3, W2, st, cols)
+    np.testing.assert_allclose(c["dW1"], gr["dW1"][:, :, cols], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(c["dW3"], gr["dW3"][:, :, cols], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(c["dW2"], gr["dW2"][:, cols, :], rtol=1e-12, atol=1e-12)
