@@ -242,6 +242,31 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* w, const void
                          const moe_saved* saved, void* dx, const moe_grads* grads, int accumulate, void* ws,
                          size_t ws_bytes, moe_stream_t stream);
 
+/* Bytes of device memory the library reserves, on every GPU that loads it and
+ * until the process exits, for moe_router_topk_noalloc. */
+#define MOE_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+/* moe_router_topk for callers that cannot allocate device memory: a plugin
+ * hosted by a program that owns every allocation, a path whose memory budget
+ * is fixed at start-up, or a latency-critical loop that cannot afford the
+ * implicit device synchronisation of cudaMalloc/cudaFree.  No workspace is
+ * passed; the routing histograms and scan live in a static device array of
+ * MOE_NOALLOC_SCRATCH_BYTES owned by the library (the pages have no
+ * counterpart of this entry point; it is a deployment convenience).
+ * Arguments, results and errors are those of moe_router_topk, plus
+ * MOE_ERR_WORKSPACE when the layer needs more than MOE_NOALLOC_SCRATCH_BYTES
+ * of scratch: 2 * E * k * ceil(T/64) * 4 bytes plus a little (E = 32, k = 4
+ * fits up to T = 65,000 tokens).  The call allocates nothing.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call on a device shares the one array and
+ * it keeps the previous call's contents (the kernels rewrite or clear all of
+ * it they read), so calls that overlap on the GPU -- on two streams, or from
+ * two host threads -- race and must be serialised by the caller. */
+moe_status moe_router_topk_noalloc(const moe_config* cfg, const void* x, const float* W_r, const float* bias,
+                                   int32_t* ids, float* gates, float* probs, int32_t* slot, int32_t* row_of,
+                                   int32_t* src_token, int32_t* counts, int32_t* offsets, moe_stream_t stream);
+
 /* Waits for the current device to finish, then reads the device error word:
  * *code is MOE_OK, MOE_ERR_DEVICE_CHECK or MOE_ERR_TIMEOUT, *detail says which
  * kernel and check; clear != 0 resets the word.  Either output may be NULL. */

@@ -63,6 +63,7 @@ _SIGNATURES = {
     "moe_max_rows": [_CFG, ctypes.POINTER(ctypes.c_int64)],
     "moe_workspace_size": [_CFG, _I, ctypes.POINTER(ctypes.c_size_t)],
     "moe_router_topk": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _Z, _P],
+    "moe_router_topk_noalloc": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_permute": [_CFG, _P, _P, _P, _P, _P, _P],
     "moe_grouped_ffn": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_unpermute_combine": [_CFG, _P, _P, _P, _P, _P],
@@ -166,6 +167,19 @@ def moe_router_topk(cfg, x, W_r, bias, ids, gates, probs, slot, row_of, src_toke
         ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(bias), _ptr(ids), _ptr(gates), _ptr(probs), _ptr(slot),
         _ptr(row_of), _ptr(src_token), _ptr(counts), _ptr(offsets), _ptr(ws), ws.numel() * ws.element_size(),
         _stream(stream)))
+
+
+def moe_router_topk_noalloc(cfg, x, W_r, bias, ids, gates, probs, slot, row_of, src_token, counts, offsets,
+                            stream=None) -> None:
+    """moe_router_topk without a workspace, for callers that cannot allocate device memory.
+
+    The library keeps the routing scratch in its own static device array
+    (MOE_NOALLOC_SCRATCH_BYTES), shared by every call on a device: do not let
+    two of these calls overlap on the GPU.
+    """
+    _check("moe_router_topk_noalloc", lib().moe_router_topk_noalloc(
+        ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(bias), _ptr(ids), _ptr(gates), _ptr(probs), _ptr(slot),
+        _ptr(row_of), _ptr(src_token), _ptr(counts), _ptr(offsets), _stream(stream)))
 
 
 def moe_permute(cfg, x, row_of, counts, offsets, x_perm, stream=None) -> None:

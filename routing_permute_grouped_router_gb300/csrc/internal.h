@@ -104,4 +104,11 @@ cudaError_t simt_ffn_fwd(const Shape& s, const FfnFwdArgs& a, uint32_t* err, cud
 cudaError_t simt_ffn_bwd(const Shape& s, const FfnBwdArgs& a, uint32_t* err, cudaStream_t st);
 bool tc_driver_ready();  // tensor-map encoder resolved from the driver
 
+// ---- moe_api.cu: shared with the allocation-free router entry point ----
+// Validates a moe_config and derives its Shape; returns a moe_status value.
+int validate_config(const void* cfg, Shape* s);
+// Device error word of the current device (checks the device is sm_103);
+// returns a moe_status value.
+int current_error_word(uint32_t** err);
+
 }  // namespace moe

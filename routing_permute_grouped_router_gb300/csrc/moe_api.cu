@@ -283,6 +283,10 @@ moe_status do_dx_router(const Shape& s, const void* x, const void* dx_perm, cons
 }
 
 }  // namespace
+
+int validate_config(const void* cfg, Shape* s) { return make_shape(static_cast<const moe_config*>(cfg), s); }
+int current_error_word(uint32_t** err) { return device_ready(err); }
+
 }  // namespace moe
 
 using namespace moe;
