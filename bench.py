@@ -29,7 +29,7 @@ if ROOT not in sys.path:
 
 DEFAULT_WORKLOAD = "top2_e8_bf16"
 METRIC = "MoE-layer tokens/s fwd & fwd+bwd; grouped-GEMM % bf16 peak; permute GB/s"
-PROFILE_FILE = os.path.join(ROOT, "profiles", "traffic_top2_e8_bf16.txt")
+PROFILE_FILE = os.path.join(ROOT, "profiles", "gemm_tc_top2_e8_bf16.md")
 KERNEL_SOURCES = {
     "gemm_up_swiglu": "gemm_tc.cu", "gemm_down": "gemm_tc.cu", "gemm_dgrad_h_swiglu_bwd": "gemm_tc.cu",
     "gemm_dgrad_x": "gemm_tc.cu", "gemm_wgrad": "gemm_tc.cu", "permute": "rows.cu", "unpermute_combine": "rows.cu",
