@@ -33,21 +33,42 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int NSTAGE = 4;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int CTRL_BYTES = 2048;
-constexpr int SMEM_BYTES = NSTAGE * STAGE_BYTES + CTRL_BYTES + 1024;  // + alignment slack
 constexpr int THREADS = 192;
+constexpr int EPI_WARPS = 4;
+constexpr int BOX_BYTES = 4096;  // one staged output box: 32 rows x 128 bytes
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr int MAX_E = 128;
+constexpr int MAX_SMEM = 232448;  // 227 KB per CTA
 
 enum Mode { M_UP = 0, M_DOWN = 1, M_DGRAD_H = 2, M_DGRAD_X = 3, M_WGRAD = 4 };
 
+// Pipeline depth and epilogue staging per product.  Each epilogue warp owns two
+// output boxes (double buffering of its TMA stores); dgrad h also stages its a
+// and b inputs, so it gives up one mainloop stage for four boxes per warp.
+template <int MODE>
+struct ModeCfg {
+  static constexpr int NST = MODE == M_DGRAD_H ? 3 : 4;
+  static constexpr int EPI_WARP_BYTES = (MODE == M_DGRAD_H ? 4 : 2) * BOX_BYTES;
+  static constexpr int EPI_OFF = NST * STAGE_BYTES;
+  static constexpr int CTRL_OFF = EPI_OFF + EPI_WARPS * EPI_WARP_BYTES;
+  static constexpr int SMEM = CTRL_OFF + CTRL_BYTES + 1024;  // + alignment slack
+};
+static_assert(ModeCfg<M_UP>::SMEM <= MAX_SMEM, "shared memory budget");
+static_assert(ModeCfg<M_DGRAD_H>::SMEM <= MAX_SMEM, "shared memory budget");
+
+// Tensor maps per product (loads of the mainloop first, then epilogue maps):
+//   UP      0 x_perm, 1 W1, 2 W3, 3 h (store), 4 a (store), 5 b (store)
+//   DOWN    0 h, 1 W2, 2 y_perm (store)
+//   DGRAD_H 0 dy_perm, 1 W2, 2 a (load), 3 b (load), 4 da (store), 5 db (store)
+//   DGRAD_X 0 da, 1 db, 2 W1, 3 W3, 4 dx_perm (store)
+//   WGRAD   0 x_perm, 1 h, 2 da, 3 db, 4 dy_perm, 5 dW1, 6 dW3, 7 dW2 (fp32 store / reduce-add)
 struct TcMaps {
-  CUtensorMap m[6];
+  CUtensorMap m[8];
 };
 
 struct TcArgs {
@@ -173,6 +194,36 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
 }
 __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) { asm volatile("" : TMEM_REGS32(r)::"memory"); }
 
+// TMA stores / reductions from shared memory, tracked with bulk groups.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(c0), "r"(c1)
+               : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(c0), "r"(c1)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// at most one bulk group may still be reading shared memory
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void sts128(uint32_t addr, const uint4& v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle, sm_100 family version bit.
 //   K-major tile: rows of 64 bf16 (128 B), 8-row atoms 1024 B apart (SBO).
 //   MN-major tile: 64 MN-contiguous bf16 per 128-B row, one row per K;
@@ -192,27 +243,45 @@ __host__ __device__ constexpr uint32_t idesc_bf16(bool a_mn, bool b_mn) {
          ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 }
 
-__device__ __forceinline__ float silu_f(float z) { return z / (1.f + __expf(-z)); }
+// silu and sigmoid with the fast intrinsic divide (about 2 ulp; the results
+// are rounded to bf16).  For z -> -inf the divisor overflows to inf and the
+// intrinsic returns 0, the right limit.
+__device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.f + __expf(-z)); }
+__device__ __forceinline__ float sigmoid_f(float z) { return __fdividef(1.f, 1.f + __expf(-z)); }
 
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&v)[32]) {
-  uint4* p = reinterpret_cast<uint4*>(dst);
+// A staged output box is 32 rows x 128 bytes (64 bf16 or 32 fp32 per row) in
+// the 128-byte swizzle the TMA expects: 16-byte chunk j of row r sits at chunk
+// j ^ (r % 8).  Boxes start on 1024-byte boundaries.  Row r belongs to lane r.
+__device__ __forceinline__ uint32_t box_chunk(uint32_t box, int lane, int j) {
+  return box + lane * 128 + (((uint32_t)j ^ (uint32_t)(lane & 7)) << 4);
+}
+__device__ __forceinline__ void box_put_bf16x32(uint32_t box, int lane, int j0, const float (&v)[32]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     float w[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) w[i] = v[8 * q + i];
-    p[q] = pack(w);
+    sts128(box_chunk(box, lane, j0 + q), pack(w));
   }
 }
-__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float (&v)[32]) {
-  const uint4* p = reinterpret_cast<const uint4*>(src);
+__device__ __forceinline__ void box_get_bf16x32(uint32_t box, int lane, int j0, float (&v)[32]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     float w[8];
-    unpack(__ldg(p + q), w);
+    unpack(lds128(box_chunk(box, lane, j0 + q)), w);
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[8 * q + i] = w[i];
   }
+}
+__device__ __forceinline__ void box_put_f32x32(uint32_t box, int lane, const float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    sts128(box_chunk(box, lane, q), make_uint4(__float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]),
+                                               __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3])));
+}
+__device__ __forceinline__ void regs_to_f32(const uint32_t (&r)[32], float (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // ------------------------------ tile schedule ------------------------------ //
@@ -309,126 +378,226 @@ __device__ __forceinline__ void issue_stage(const TcMaps& maps, const TcArgs& a,
 }
 
 // ------------------------------ epilogues --------------------------------- //
+// Each epilogue warp owns TMEM lanes q*32 .. q*32+31 (rows of the tile) and a
+// private staging area in shared memory.  It moves 32-column slices out of
+// TMEM with tcgen05.ld, applies the fused math, writes the result into a
+// swizzled box and lets the TMA store it (or add it, for accumulated fp32
+// gradients); two boxes alternate so the next box is filled while the
+// previous one drains.
+struct EpiState {
+  uint32_t nbox;     // boxes this warp has staged so far (selects the buffer)
+  uint32_t uses[2];  // completed waits on the two input barriers (dgrad h)
+  bool pending[2];   // an input load is in flight into buffer h (dgrad h)
+};
+
+// Stage and store one bf16 output box of 64 columns taken from 2 TMEM slices.
+__device__ __forceinline__ void stage_wait(int lane) {
+  if (lane == 0) bulk_wait_read1();
+  __syncwarp();
+}
+__device__ __forceinline__ void box_issue_store(const CUtensorMap* map, uint32_t buf, int c0, int c1, int lane) {
+  fence_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(map, buf, c0, c1);
+    bulk_commit();
+  }
+}
+
 template <int MODE>
-__device__ __forceinline__ void epilogue_tile(const TcArgs& a, const Tile& t, uint32_t tacc, int q, int lane) {
-  const int64_t row = t.row0 + q * 32 + lane;
+__device__ __forceinline__ bool epilogue_tile(const TcMaps& maps, const TcArgs& a, const Tile& t, uint32_t tacc,
+                                              int q, int lane, uint32_t ebuf, uint32_t lbar, EpiState& es,
+                                              uint32_t tfull, uint32_t tfull_parity, volatile int* abort_flag) {
+  const int row0 = static_cast<int>(t.row0) + q * 32;
+  if (MODE == M_DGRAD_H) {
+    // fetch the first a/b boxes of the tile while its mainloop still runs
+    const uint32_t h = es.nbox & 1;
+    if (lane == 0) {
+      bulk_wait_read0();
+      const uint32_t bar = lbar + 8 * h;
+      mbar_expect_tx(bar, 2 * BOX_BYTES);
+      tma_load_2d(ebuf + h * 2 * BOX_BYTES, &maps.m[2], bar, t.n0, row0);
+      tma_load_2d(ebuf + h * 2 * BOX_BYTES + BOX_BYTES, &maps.m[3], bar, t.n0, row0);
+    }
+    es.pending[h] = true;
+    __syncwarp();
+  }
+  if (!mbar_wait(tfull, tfull_parity, abort_flag, a.err, 400 + MODE)) return false;
+  tc_fence_after();
+
   if (MODE == M_UP) {
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-      uint32_t ra[32], rb[32];
-      tmem_ld32(tacc + c * 32, ra);
-      tmem_ld32(tacc + 128 + c * 32, rb);
-      tmem_ld_wait(ra);
-      reg_fence(rb);
-      float hv[32], av[32], bv[32];
+    for (int c = 0; c < 2; ++c) {  // h = silu(a) * b, 64 columns per box
+      const uint32_t buf = ebuf + (es.nbox & 1) * BOX_BYTES;
+      stage_wait(lane);
+#pragma unroll 1
+      for (int s = 0; s < 2; ++s) {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(tacc + c * 64 + s * 32, ra);
+        tmem_ld32(tacc + 128 + c * 64 + s * 32, rb);
+        tmem_ld_wait(ra);
+        reg_fence(rb);
+        float hv[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        av[i] = __uint_as_float(ra[i]);
-        bv[i] = __uint_as_float(rb[i]);
-        hv[i] = silu_f(av[i]) * bv[i];
+        for (int i = 0; i < 32; ++i) hv[i] = silu_f(__uint_as_float(ra[i])) * __uint_as_float(rb[i]);
+        box_put_bf16x32(buf, lane, 4 * s, hv);
       }
-      const int64_t o = row * a.f + t.n0 + c * 32;
-      store_bf16x32(a.o0 + o, hv);
-      if (a.o1 != nullptr) store_bf16x32(a.o1 + o, av);
-      if (a.o2 != nullptr) store_bf16x32(a.o2 + o, bv);
+      box_issue_store(&maps.m[3], buf, t.n0 + c * 64, row0, lane);
+      ++es.nbox;
+    }
+#pragma unroll 1
+    for (int which = 0; which < 2; ++which) {  // a and b themselves, kept for the backward
+      if ((which == 0 ? a.o1 : a.o2) == nullptr) continue;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        const uint32_t buf = ebuf + (es.nbox & 1) * BOX_BYTES;
+        stage_wait(lane);
+#pragma unroll 1
+        for (int s = 0; s < 2; ++s) {
+          uint32_t r[32];
+          tmem_ld32(tacc + which * 128 + c * 64 + s * 32, r);
+          tmem_ld_wait(r);
+          float v[32];
+          regs_to_f32(r, v);
+          box_put_bf16x32(buf, lane, 4 * s, v);
+        }
+        box_issue_store(&maps.m[4 + which], buf, t.n0 + c * 64, row0, lane);
+        ++es.nbox;
+      }
     }
   } else if (MODE == M_DOWN || MODE == M_DGRAD_X) {
+    const CUtensorMap* om = MODE == M_DOWN ? &maps.m[2] : &maps.m[4];
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
-      uint32_t r[32];
-      tmem_ld32(tacc + c * 32, r);
-      tmem_ld_wait(r);
-      float v[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-      store_bf16x32(a.o0 + row * a.d + t.n0 + c * 32, v);
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t buf = ebuf + (es.nbox & 1) * BOX_BYTES;
+      stage_wait(lane);
+#pragma unroll 1
+      for (int s = 0; s < 2; ++s) {
+        uint32_t r[32];
+        tmem_ld32(tacc + c * 64 + s * 32, r);
+        tmem_ld_wait(r);
+        float v[32];
+        regs_to_f32(r, v);
+        box_put_bf16x32(buf, lane, 4 * s, v);
+      }
+      box_issue_store(om, buf, t.n0 + c * 64, row0, lane);
+      ++es.nbox;
     }
   } else if (MODE == M_DGRAD_H) {
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
-      uint32_t r[32];
-      tmem_ld32(tacc + c * 32, r);
-      const int64_t o = row * a.f + t.n0 + c * 32;
-      float av[32], bv[32];
-      load_bf16x32(a.i0 + o, av);
-      load_bf16x32(a.i1 + o, bv);
-      tmem_ld_wait(r);
-      float dav[32], dbv[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float dh = __uint_as_float(r[i]);
-        const float s = 1.f / (1.f + __expf(-av[i]));
-        dav[i] = dh * bv[i] * s * (1.f + av[i] * (1.f - s));
-        dbv[i] = dh * av[i] * s;
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t h = (es.nbox + c) & 1;
+      const uint32_t buf = ebuf + h * 2 * BOX_BYTES;  // [a box | b box], overwritten with [da | db]
+      if (c + 1 < 4) {
+        const uint32_t hn = h ^ 1u;
+        if (lane == 0) {
+          bulk_wait_read0();  // the stores that last used buffer hn have read it
+          const uint32_t bar = lbar + 8 * hn;
+          mbar_expect_tx(bar, 2 * BOX_BYTES);
+          tma_load_2d(ebuf + hn * 2 * BOX_BYTES, &maps.m[2], bar, t.n0 + (c + 1) * 64, row0);
+          tma_load_2d(ebuf + hn * 2 * BOX_BYTES + BOX_BYTES, &maps.m[3], bar, t.n0 + (c + 1) * 64, row0);
+        }
+        es.pending[hn] = true;
       }
-      store_bf16x32(a.o0 + o, dav);
-      store_bf16x32(a.o1 + o, dbv);
+      if (!mbar_wait(lbar + 8 * h, es.uses[h] & 1u, abort_flag, a.err, 500)) return false;
+      ++es.uses[h];
+      es.pending[h] = false;
+      uint32_t r0[32], r1[32];
+      tmem_ld32(tacc + c * 64, r0);
+      tmem_ld32(tacc + c * 64 + 32, r1);
+      tmem_ld_wait(r0);
+      reg_fence(r1);
+#pragma unroll 1
+      for (int s = 0; s < 2; ++s) {
+        float av[32], bv[32], dav[32], dbv[32];
+        box_get_bf16x32(buf, lane, 4 * s, av);
+        box_get_bf16x32(buf + BOX_BYTES, lane, 4 * s, bv);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float dh = __uint_as_float(s == 0 ? r0[i] : r1[i]);
+          const float sg = sigmoid_f(av[i]);
+          dav[i] = dh * bv[i] * sg * (1.f + av[i] * (1.f - sg));
+          dbv[i] = dh * av[i] * sg;
+        }
+        box_put_bf16x32(buf, lane, 4 * s, dav);
+        box_put_bf16x32(buf + BOX_BYTES, lane, 4 * s, dbv);
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(&maps.m[4], buf, t.n0 + c * 64, row0);
+        tma_store_2d(&maps.m[5], buf + BOX_BYTES, t.n0 + c * 64, row0);
+        bulk_commit();
+      }
     }
-  } else {  // WGRAD: fp32 rows of the weight gradient
-    const int M = t.sub == 2 ? a.f : a.d, N = t.sub == 2 ? a.d : a.f;
-    float* out = t.sub == 0 ? a.w0 : (t.sub == 1 ? a.w1 : a.w2);
-    float* dst = out + ((int64_t)t.e * M + t.m0 + q * 32 + lane) * N + t.n0;
+    es.nbox += 4;
+  } else {  // WGRAD: fp32 weight-gradient rows, stored or added in place
+    if (t.kblocks == 0 && a.accumulate) return true;
+    const int M = t.sub == 2 ? a.f : a.d;
+    const CUtensorMap* om = &maps.m[5 + t.sub];
+    const int orow = t.e * M + t.m0 + q * 32;
 #pragma unroll 1
     for (int c = 0; c < 8; ++c) {
+      const uint32_t buf = ebuf + (es.nbox & 1) * BOX_BYTES;
+      stage_wait(lane);
       float v[32];
       if (t.kblocks > 0) {
         uint32_t r[32];
         tmem_ld32(tacc + c * 32, r);
         tmem_ld_wait(r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+        regs_to_f32(r, v);
       } else {
-        if (a.accumulate) continue;
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = 0.f;
       }
-      float4* p = reinterpret_cast<float4*>(dst + c * 32);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        float4 w = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-        if (a.accumulate) {
-          const float4 old = p[i];
-          w.x += old.x;
-          w.y += old.y;
-          w.z += old.z;
-          w.w += old.w;
-        }
-        p[i] = w;
+      box_put_f32x32(buf, lane, v);
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        if (a.accumulate) tma_reduce_add_2d(om, buf, t.n0 + c * 32, orow);
+        else tma_store_2d(om, buf, t.n0 + c * 32, orow);
+        bulk_commit();
       }
+      ++es.nbox;
     }
   }
+  return true;
 }
 
 // ------------------------------ the kernel -------------------------------- //
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcMaps maps,
                                                              const __grid_constant__ TcArgs a) {
+  using Cfg = ModeCfg<MODE>;
+  constexpr int NST = Cfg::NST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* ctrl = smem + NSTAGE * STAGE_BYTES;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(ctrl);
-  uint64_t* empty_bar = full_bar + NSTAGE;
-  uint64_t* tfull_bar = empty_bar + NSTAGE;
-  uint64_t* tempty_bar = tfull_bar + 2;
-  uint64_t* drain_bar = tempty_bar + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  uint8_t* ctrl = smem + Cfg::CTRL_OFF;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(ctrl);        // [NST]
+  uint64_t* empty_bar = full_bar + 4;                             // [NST]
+  uint64_t* tfull_bar = empty_bar + 4;                            // [2]
+  uint64_t* tempty_bar = tfull_bar + 2;                           // [2]
+  uint64_t* drain_bar = tempty_bar + 2;                           // [1]
+  uint64_t* load_bar = drain_bar + 1;                             // [EPI_WARPS][2] (dgrad h inputs)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(load_bar + 2 * EPI_WARPS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_total = reinterpret_cast<int*>(tmem_slot + 2);
-  int* s_off = reinterpret_cast<int*>(ctrl + 128);        // E + 1 ints
-  int* s_cnt = s_off + MAX_E + 1;                         // E ints
+  int* s_off = reinterpret_cast<int*>(ctrl + 256);  // E + 1 ints
+  int* s_cnt = s_off + MAX_E + 1;                   // E ints
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NSTAGE; ++i) {
+    for (int i = 0; i < NST; ++i) {
       mbar_init(smem_addr(&full_bar[i]), 1);
       mbar_init(smem_addr(&empty_bar[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_addr(&tfull_bar[i]), 1);
-      mbar_init(smem_addr(&tempty_bar[i]), 4);
+      mbar_init(smem_addr(&tempty_bar[i]), EPI_WARPS);
     }
     mbar_init(smem_addr(drain_bar), 1);
+    for (int i = 0; i < 2 * EPI_WARPS; ++i) mbar_init(smem_addr(&load_bar[i]), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -466,8 +635,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer ----------------
-      constexpr int NMAPS = MODE == M_UP ? 3 : (MODE == M_DGRAD_X ? 4 : (MODE == M_WGRAD ? 5 : 2));
-      for (int i = 0; i < NMAPS; ++i) prefetch_map(&maps.m[i]);
+      constexpr int NLOAD = MODE == M_UP ? 3 : (MODE == M_DGRAD_X ? 4 : (MODE == M_WGRAD ? 5 : 2));
+      for (int i = 0; i < NLOAD; ++i) prefetch_map(&maps.m[i]);
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
@@ -484,7 +653,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
           const uint32_t sA = smem_base + stage * STAGE_BYTES;
           issue_stage<MODE>(maps, a, t, kb, sA, sA + A_BYTES, fb);
           ++issued;
-          if (++stage == NSTAGE) {
+          if (++stage == NST) {
             stage = 0;
             phase ^= 1u;
           }
@@ -492,12 +661,12 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
       }
       if (!alive) {
         // drain the copies still in flight before the CTA may exit
-        int n = issued < NSTAGE ? issued : NSTAGE;
+        const int n = issued < NST ? issued : NST;
         int s = stage;
         uint32_t ph = phase;
         for (int i = 0; i < n; ++i) {
           if (--s < 0) {
-            s = NSTAGE - 1;
+            s = NST - 1;
             ph ^= 1u;
           }
           const uint32_t fb = smem_addr(&full_bar[s]);
@@ -538,7 +707,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
             umma_bf16(d_tmem, ad, bd, IDESC, (kb | k16) != 0 ? 1u : 0u);
           }
           umma_commit(smem_addr(&empty_bar[stage]));
-          if (++stage == NSTAGE) {
+          if (++stage == NST) {
             stage = 0;
             phase ^= 1u;
           }
@@ -554,19 +723,29 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
   } else {
     // ---------------- epilogue warps 2..5 ----------------
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int ew = warp - 2;
+    const uint32_t ebuf = smem_base + Cfg::EPI_OFF + ew * Cfg::EPI_WARP_BYTES;
+    const uint32_t lbar = smem_addr(&load_bar[2 * ew]);
+    EpiState es{0u, {0u, 0u}, {false, false}};
     int local = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
       const Tile t = decode<MODE>(tile, a, s_off, s_cnt);
       const int acc = local & 1;
       const uint32_t use = (uint32_t)(local >> 1) & 1u;
-      if (!mbar_wait(smem_addr(&tfull_bar[acc]), use, abort_flag, a.err, 400 + MODE)) break;
-      tc_fence_after();
       const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-      epilogue_tile<MODE>(a, t, tacc, q, lane);
+      if (!epilogue_tile<MODE>(maps, a, t, tacc, q, lane, ebuf, lbar, es, smem_addr(&tfull_bar[acc]), use,
+                               abort_flag))
+        break;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&tempty_bar[acc]));
     }
+    // input loads still in flight (only after an abort), then every store
+    for (int h = 0; h < 2; ++h)
+      if (es.pending[h])
+        for (uint32_t it = 0; it < (1u << 24) && !mbar_try_wait(lbar + 8 * h, es.uses[h] & 1u); ++it) {
+        }
+    if (lane == 0) bulk_wait_all();
   }
   __syncwarp();
 
@@ -593,15 +772,17 @@ bool resolve_encode() {
   return g_encode != nullptr;
 }
 
-// 2-D bf16 tensor map over a row-major [rows, cols] matrix, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
-              uint32_t box_rows) {
+// 2-D tensor map over a row-major [rows, cols] matrix, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows,
+              bool fp32 = false) {
+  const uint64_t es = fp32 ? 4 : 2;
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
+  cuuint64_t strides[1] = {cols * es};
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return g_encode(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -625,15 +806,15 @@ cudaError_t launch_mode(const TcMaps& maps, const TcArgs& args, int64_t tile_bou
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
   if (!attr_done[dev]) {
-    cudaError_t e =
-        cudaFuncSetAttribute(tc_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         ModeCfg<MODE>::SMEM);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
   if (tile_bound <= 0) return cudaSuccess;
   const int grid = (int)(tile_bound < num_sms() ? tile_bound : num_sms());
   LaunchScope ls(kind, st);
-  tc_gemm_kernel<MODE><<<grid, THREADS, SMEM_BYTES, st>>>(maps, args);
+  tc_gemm_kernel<MODE><<<grid, THREADS, ModeCfg<MODE>::SMEM, st>>>(maps, args);
   return cudaGetLastError();
 }
 
@@ -655,8 +836,11 @@ cudaError_t tc_ffn_fwd(const Shape& s, const FfnFwdArgs& f, uint32_t* err, cudaS
   a.err = err;
   TcMaps up{}, down{};
   bool ok = make_map(&up.m[0], f.x_perm, R, d, 64, BM) && make_map(&up.m[1], f.W1, E * d, ff, 64, 64) &&
-            make_map(&up.m[2], f.W3, E * d, ff, 64, 64);
-  ok = ok && make_map(&down.m[0], f.h, R, ff, 64, BM) && make_map(&down.m[1], f.W2, E * ff, d, 64, 64);
+            make_map(&up.m[2], f.W3, E * d, ff, 64, 64) && make_map(&up.m[3], f.h, R, ff, 64, 32);
+  if (f.a != nullptr) ok = ok && make_map(&up.m[4], f.a, R, ff, 64, 32);
+  if (f.b != nullptr) ok = ok && make_map(&up.m[5], f.b, R, ff, 64, 32);
+  ok = ok && make_map(&down.m[0], f.h, R, ff, 64, BM) && make_map(&down.m[1], f.W2, E * ff, d, 64, 64) &&
+       make_map(&down.m[2], f.y_perm, R, d, 64, 32);
   if (!ok) return cudaErrorInvalidValue;
   const int64_t mt = s.max_rows / BM;
   a.o0 = static_cast<__nv_bfloat16*>(f.h);
@@ -690,12 +874,16 @@ cudaError_t tc_ffn_bwd(const Shape& s, const FfnBwdArgs& b, uint32_t* err, cudaS
   a.err = err;
   a.accumulate = b.accumulate;
   TcMaps mh{}, mw{}, mx{};
-  bool ok = make_map(&mh.m[0], b.dy_perm, R, d, 64, BM) && make_map(&mh.m[1], b.W2, E * ff, d, 64, BN);
+  bool ok = make_map(&mh.m[0], b.dy_perm, R, d, 64, BM) && make_map(&mh.m[1], b.W2, E * ff, d, 64, BN) &&
+            make_map(&mh.m[2], b.a, R, ff, 64, 32) && make_map(&mh.m[3], b.b, R, ff, 64, 32) &&
+            make_map(&mh.m[4], b.da, R, ff, 64, 32) && make_map(&mh.m[5], b.db, R, ff, 64, 32);
   ok = ok && make_map(&mw.m[0], b.x_perm, R, d, 64, 64) && make_map(&mw.m[1], b.h, R, ff, 64, 64) &&
        make_map(&mw.m[2], b.da, R, ff, 64, 64) && make_map(&mw.m[3], b.db, R, ff, 64, 64) &&
-       make_map(&mw.m[4], b.dy_perm, R, d, 64, 64);
+       make_map(&mw.m[4], b.dy_perm, R, d, 64, 64) && make_map(&mw.m[5], b.dW1, E * d, ff, 32, 32, true) &&
+       make_map(&mw.m[6], b.dW3, E * d, ff, 32, 32, true) && make_map(&mw.m[7], b.dW2, E * ff, d, 32, 32, true);
   ok = ok && make_map(&mx.m[0], b.da, R, ff, 64, BM) && make_map(&mx.m[1], b.db, R, ff, 64, BM) &&
-       make_map(&mx.m[2], b.W1, E * d, ff, 64, BN) && make_map(&mx.m[3], b.W3, E * d, ff, 64, BN);
+       make_map(&mx.m[2], b.W1, E * d, ff, 64, BN) && make_map(&mx.m[3], b.W3, E * d, ff, 64, BN) &&
+       make_map(&mx.m[4], b.dx_perm, R, d, 64, 32);
   if (!ok) return cudaErrorInvalidValue;
   const int64_t mt = s.max_rows / BM;
   a.o0 = static_cast<__nv_bfloat16*>(b.da);
