@@ -25,6 +25,7 @@ enum KernelKind : int {
   KK_DWR_PARTIAL,
   KK_DWR_REDUCE,
   KK_ZERO,
+  KK_SPLIT_WR,
   KK_COUNT
 };
 
@@ -68,6 +69,13 @@ cudaError_t launch_slot_assign(const Shape& s, const int32_t* ids, const int32_t
                                const int32_t* offsets, int32_t* slot, int32_t* row_of, int32_t* src_token,
                                uint32_t* err, cudaStream_t st);
 int router_blocks(int T);  // tokens per router block is fixed; this is the block count
+
+// ---- router_tc.cu: tensor-core router for bf16 layers with T >= 128 ----
+bool router_tc_supported(const Shape& s);
+size_t router_wsplit_bytes(const Shape& s);  // scratch for the three bf16 parts of W_r
+cudaError_t launch_router_tc(const Shape& s, const void* x, const float* W_r, const float* bias, void* wsplit,
+                             int32_t* ids, float* gates, float* probs, int32_t* hist, int32_t* ticket,
+                             uint32_t* err, cudaStream_t st);
 
 // ---- rows.cu ----
 cudaError_t launch_permute(const Shape& s, const void* x, const int32_t* row_of, const int32_t* counts,

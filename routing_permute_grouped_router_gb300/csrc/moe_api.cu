@@ -76,7 +76,7 @@ cudaEvent_t pool_event() {
 const char* const kKernelNames[KK_COUNT] = {
     "router_topk",  "slot_scan",  "slot_assign",     "permute",      "gemm_up_swiglu", "gemm_down",
     "unpermute_combine", "combine_bwd", "gemm_dgrad_h_swiglu_bwd", "gemm_wgrad", "gemm_dgrad_x",
-    "transpose_wr", "dx_router",  "dwr_partial",     "dwr_reduce",   "zero"};
+    "transpose_wr", "dx_router",  "dwr_partial",     "dwr_reduce",   "zero", "split_wr"};
 
 }  // namespace
 
@@ -177,6 +177,7 @@ struct RoutingScratch {
   int32_t* base;
   int32_t* totals;
   int32_t* ticket;
+  void* wsplit;  // bf16 parts of W_r for the tensor-core router
 };
 struct FwdScratch {
   int32_t *ids, *slot, *row_of, *src_token, *counts, *offsets;
@@ -195,6 +196,7 @@ RoutingScratch carve_routing(Carver& c, const Shape& s) {
   r.base = static_cast<int32_t*>(c.take(n * 4));
   r.totals = static_cast<int32_t*>(c.take((size_t)s.E * 4));
   r.ticket = static_cast<int32_t*>(c.take(4));
+  r.wsplit = c.take(router_wsplit_bytes(s));
   return r;
 }
 FwdScratch carve_fwd(Carver& c, const Shape& s) {
@@ -245,7 +247,10 @@ moe_status do_router(const Shape& s, const void* x, const float* W_r, const floa
     CUDA_TRY(cudaMemsetAsync(offsets, 0, (size_t)(s.E + 1) * 4, st));
     return MOE_OK;
   }
-  CUDA_TRY(launch_router(s, x, W_r, bias, ids, gates, probs, rs.hist, rs.ticket, st));
+  if (router_tc_supported(s))
+    CUDA_TRY(launch_router_tc(s, x, W_r, bias, rs.wsplit, ids, gates, probs, rs.hist, rs.ticket, err, st));
+  else
+    CUDA_TRY(launch_router(s, x, W_r, bias, ids, gates, probs, rs.hist, rs.ticket, st));
   CUDA_TRY(launch_slot_scan(s, rs.hist, rs.base, rs.totals, rs.ticket, counts, offsets, err, st));
   CUDA_TRY(launch_slot_assign(s, ids, rs.base, counts, offsets, slot, row_of, src_token, err, st));
   return MOE_OK;

@@ -1,0 +1,376 @@
+// Router scoring on the tensor cores: logits = x W_r + b, then fp32 softmax,
+// top-k and the per-block expert histogram, for bf16 layers.
+//
+// "The router scores every token" (gpu_expert_parallel page, step timeline)
+// is a skinny product, T x d by d x E, that must come out in fp32 precision
+// (the layer configurations fix an fp32 router).  x is exact in bf16; W_r is
+// split into three bf16 parts, hi + mid + lo, which together carry its 24
+// significand bits (the bf16x3 technique of Henry, Tang and Heinecke,
+// "Leveraging the bfloat16 AI datatype for higher-precision computations",
+// 2019).  Each product x * part is exact in the fp32 accumulator, so three
+// MMAs per K step give fp32-accurate logits while reading x from HBM once at
+// TMA speed.
+//
+// One CTA per 128-token tile: warp 0 lane 0 loads 128x64 x tiles and the three
+// E_pad x 64 weight tiles with TMA, warp 1 lane 0 issues tcgen05.mma
+// (M=128, N=E_pad, K=16) into an fp32 TMEM accumulator, and warps 2-5 read one
+// token row per thread from TMEM and do softmax and top-k in registers (value
+// descending, lower expert index on ties).  The histogram is written per
+// 64-token block, the layout the slot scan reads.
+#include <cudaTypedefs.h>
+#include <float.h>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int RT = 128;  // tokens per tile
+constexpr int RK = 64;   // K per stage (128-byte rows)
+constexpr int HIST_TOK = 64;
+constexpr int R_THREADS = 192;
+constexpr int R_MAXK = 8;
+
+template <int N>
+struct RCfg {
+  static constexpr int NST = N <= 64 ? 4 : 3;
+  static constexpr int A_BYTES = RT * RK * 2;
+  static constexpr int B_BYTES = 3 * N * RK * 2;
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int CTRL_OFF = NST * STAGE;
+  static constexpr int SMEM = CTRL_OFF + 256 + 1024;
+  static constexpr uint32_t TCOLS = N < 32 ? 32 : N;
+  // fp32 D, bf16 A and B, both K-major, M = 128, N
+  static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+                                    ((uint32_t)(RT >> 4) << 24);
+};
+
+struct RouterTcArgs {
+  const float* bias;
+  int32_t* ids;
+  float* gates;
+  float* probs;
+  int32_t* hist;
+  int32_t* ticket;
+  uint32_t* err;
+  int T, d, E, k, nb;
+};
+
+// W_r [d, E] fp32 -> wsplit [3][N][d] bf16 (hi, mid, lo; rows e >= E are zero).
+__global__ void split_wr_kernel(const float* W_r, __nv_bfloat16* wsplit, int d, int E, int N) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (int64_t)N * d) return;
+  const int e = (int)(i / d), c = (int)(i % d);
+  const float w = e < E ? W_r[(size_t)c * E + e] : 0.f;
+  const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+  const float r1 = w - __bfloat162float(hi);
+  const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+  const float r2 = r1 - __bfloat162float(mid);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
+  const size_t plane = (size_t)N * d;
+  wsplit[i] = hi;
+  wsplit[plane + i] = mid;
+  wsplit[2 * plane + i] = lo;
+}
+
+template <int N>
+__global__ void __launch_bounds__(R_THREADS, 1) router_tc_kernel(const __grid_constant__ CUtensorMap map_x,
+                                                                 const __grid_constant__ CUtensorMap map_w,
+                                                                 const __grid_constant__ RouterTcArgs a) {
+  using C = RCfg<N>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int hist_s[2][R_MAXK][N];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::CTRL_OFF);
+  uint64_t* empty_bar = full_bar + 4;
+  uint64_t* tfull_bar = empty_bar + 4;
+  uint64_t* drain_bar = tfull_bar + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int tile = blockIdx.x;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NST; ++i) {
+      mbar_init(smem_addr(&full_bar[i]), 1);
+      mbar_init(smem_addr(&empty_bar[i]), 1);
+    }
+    mbar_init(smem_addr(tfull_bar), 1);
+    mbar_init(smem_addr(drain_bar), 1);
+    *abort_flag = 0;
+    if (tile == 0) *a.ticket = 0;  // for the last-block election of the slot scan
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  for (int i = threadIdx.x; i < 2 * R_MAXK * N; i += R_THREADS) (&hist_s[0][0][0])[i] = 0;
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), C::TCOLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t smem_base = smem_addr(smem);
+  const int kblocks = a.d / RK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_map(&map_x);
+      prefetch_map(&map_w);
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      bool alive = true;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!mbar_wait(smem_addr(&empty_bar[stage]), phase ^ 1u, abort_flag, a.err, 600)) {
+          alive = false;
+          break;
+        }
+        const uint32_t fb = smem_addr(&full_bar[stage]);
+        mbar_expect_tx(fb, C::STAGE);
+        const uint32_t sA = smem_base + stage * C::STAGE;
+        tma_load_2d(sA, &map_x, fb, kb * RK, tile * RT);
+#pragma unroll
+        for (int s = 0; s < 3; ++s) tma_load_2d(sA + C::A_BYTES + s * N * 128, &map_w, fb, kb * RK, s * N);
+        ++issued;
+        if (++stage == C::NST) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!alive) {
+        const int n = issued < C::NST ? issued : C::NST;
+        int s = stage;
+        uint32_t ph = phase;
+        for (int i = 0; i < n; ++i) {
+          if (--s < 0) {
+            s = C::NST - 1;
+            ph ^= 1u;
+          }
+          for (uint32_t it = 0; it < (1u << 24) && !mbar_try_wait(smem_addr(&full_bar[s]), ph); ++it) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool alive = true;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!mbar_wait(smem_addr(&full_bar[stage]), phase, abort_flag, a.err, 601)) {
+          alive = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sA = smem_base + stage * C::STAGE;
+        const uint32_t sB = sA + C::A_BYTES;
+#pragma unroll
+        for (int k16 = 0; k16 < RK / 16; ++k16) {
+          const uint64_t ad = sdesc(sA + k16 * 32, 16, 1024);
+#pragma unroll
+          for (int s = 0; s < 3; ++s)
+            umma_bf16(tmem_base, ad, sdesc(sB + s * N * 128 + k16 * 32, 16, 1024), C::IDESC,
+                      (kb | k16 | s) != 0 ? 1u : 0u);
+        }
+        umma_commit(smem_addr(&empty_bar[stage]));
+        if (++stage == C::NST) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (alive) umma_commit(smem_addr(tfull_bar));
+      umma_commit(smem_addr(drain_bar));
+      for (uint32_t it = 0; it < (1u << 26) && !mbar_try_wait(smem_addr(drain_bar), 0); ++it) {
+      }
+    }
+  } else {
+    // ---- epilogue: one token per thread ----
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const int t = tile * RT + row;
+    if (mbar_wait(smem_addr(tfull_bar), 0, abort_flag, a.err, 602)) {
+      tc_fence_after();
+      float v[N];
+#pragma unroll
+      for (int c = 0; c < N / 16; ++c) {
+        uint32_t r[16];
+        tmem_ld16(tmem_base + ((uint32_t)(q * 32) << 16) + c * 16, r);
+        tmem_ld_wait16(r);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[c * 16 + i] = __uint_as_float(r[i]);
+      }
+      if (t < a.T) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+          float l = -INFINITY;
+          if (e < a.E) {
+            l = v[e] + (a.bias != nullptr ? __ldg(a.bias + e) : 0.f);
+            if (isnan(l)) l = -INFINITY;
+          }
+          v[e] = l;
+          mx = fmaxf(mx, l);
+        }
+        float se = 0.f;
+#pragma unroll
+        for (int e = 0; e < N; ++e)
+          if (e < a.E) se += expf(v[e] - mx);
+        if (a.probs != nullptr) {
+          float* pr = a.probs + (size_t)t * a.E;
+#pragma unroll
+          for (int e = 0; e < N; ++e)
+            if (e < a.E) pr[e] = expf(v[e] - mx) / se;
+        }
+        float lj[R_MAXK];
+        int ej[R_MAXK];
+#pragma unroll
+        for (int j = 0; j < R_MAXK; ++j) {
+          lj[j] = 0.f;
+          ej[j] = 0;
+          if (j < a.k) {
+            float bv = -INFINITY;
+            int be = -1;
+#pragma unroll
+            for (int e = 0; e < N; ++e)
+              if (e < a.E && (be < 0 || v[e] > bv)) {  // strict: the lower index wins ties
+                bv = v[e];
+                be = e;
+              }
+#pragma unroll
+            for (int e = 0; e < N; ++e)
+              if (e == be) v[e] = -INFINITY;
+            // a taken expert is -inf; if every remaining logit is -inf the
+            // lowest untaken index still has to be found
+            if (bv == -INFINITY) {
+              be = -1;
+              for (int e = 0; e < a.E && be < 0; ++e) {
+                bool used = false;
+                for (int jj = 0; jj < j; ++jj) used |= ej[jj] == e;
+                if (!used) be = e;
+              }
+            }
+            lj[j] = bv;
+            ej[j] = be;
+          }
+        }
+        float g[R_MAXK];
+        if (a.k == 1) {
+          g[0] = expf(lj[0] - mx) / se;
+        } else {
+          float den = 0.f;
+#pragma unroll
+          for (int j = 0; j < R_MAXK; ++j)
+            if (j < a.k) {
+              g[j] = expf(lj[j] - lj[0]);
+              den += g[j];
+            }
+#pragma unroll
+          for (int j = 0; j < R_MAXK; ++j)
+            if (j < a.k) g[j] = g[j] / den;
+        }
+        const int half = row / HIST_TOK;
+#pragma unroll
+        for (int j = 0; j < R_MAXK; ++j)
+          if (j < a.k) {
+            a.ids[(size_t)t * a.k + j] = ej[j];
+            a.gates[(size_t)t * a.k + j] = g[j];
+            atomicAdd(&hist_s[half][j][ej[j]], 1);
+          }
+      }
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // histogram of the two 64-token blocks of this tile, laid out [e][j][block]
+  for (int i = threadIdx.x; i < 2 * a.k * a.E; i += R_THREADS) {
+    const int half = i / (a.k * a.E), r = i % (a.k * a.E), j = r / a.E, e = r % a.E;
+    const int b = tile * 2 + half;
+    if (b < a.nb) a.hist[((size_t)e * a.k + j) * a.nb + b] = hist_s[half][j][e];
+  }
+  if (warp == 1) tmem_dealloc(tmem_base, C::TCOLS);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 r_encode = nullptr;
+
+bool router_encode_ready() {
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      r_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return r_encode != nullptr;
+}
+
+bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                   uint32_t box_rows) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return r_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int padded_experts(int E) { return E <= 16 ? 16 : (E <= 32 ? 32 : (E <= 64 ? 64 : 128)); }
+
+template <int N>
+cudaError_t launch_n(const CUtensorMap& mx, const CUtensorMap& mw, const RouterTcArgs& args, int tiles,
+                     cudaStream_t st) {
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!attr_done[dev]) {
+    cudaError_t e =
+        cudaFuncSetAttribute(router_tc_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, RCfg<N>::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  LaunchScope ls(KK_ROUTER, st);
+  router_tc_kernel<N><<<tiles, R_THREADS, RCfg<N>::SMEM, st>>>(mx, mw, args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool router_tc_supported(const Shape& s) { return s.bf16 && s.T >= RT && s.d % RK == 0 && s.E <= 128; }
+
+size_t router_wsplit_bytes(const Shape& s) { return (size_t)3 * padded_experts(s.E) * s.d * 2; }
+
+cudaError_t launch_router_tc(const Shape& s, const void* x, const float* W_r, const float* bias, void* wsplit,
+                             int32_t* ids, float* gates, float* probs, int32_t* hist, int32_t* ticket,
+                             uint32_t* err, cudaStream_t st) {
+  if (!router_encode_ready()) return cudaErrorNotSupported;
+  const int N = padded_experts(s.E);
+  {
+    const int64_t n = (int64_t)N * s.d;
+    LaunchScope ls(KK_SPLIT_WR, st);
+    split_wr_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(W_r, static_cast<__nv_bfloat16*>(wsplit), s.d,
+                                                                  s.E, N);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  CUtensorMap mx, mw;
+  if (!make_map_bf16(&mx, x, (uint64_t)s.T, (uint64_t)s.d, RK, RT) ||
+      !make_map_bf16(&mw, wsplit, (uint64_t)3 * N, (uint64_t)s.d, RK, (uint32_t)N))
+    return cudaErrorInvalidValue;
+  RouterTcArgs a{bias, ids, gates, probs, hist, ticket, err, s.T, s.d, s.E, s.k, router_blocks(s.T)};
+  const int tiles = (s.T + RT - 1) / RT;
+  switch (N) {
+    case 16: return launch_n<16>(mx, mw, a, tiles, st);
+    case 32: return launch_n<32>(mx, mw, a, tiles, st);
+    case 64: return launch_n<64>(mx, mw, a, tiles, st);
+    default: return launch_n<128>(mx, mw, a, tiles, st);
+  }
+}
+
+}  // namespace moe
