@@ -282,6 +282,10 @@ uint64_t moe_launch_count(void);
  * moe_kernel_kinds(), the launches and total milliseconds. */
 moe_status moe_profiler_enable(int on);
 int32_t moe_kernel_kinds(void);
+/* Restricts the profiler to launches of kernel kind id (0 <= id <
+ * moe_kernel_kinds()), or to every kind when id < 0 (the default).  Applies to
+ * launches issued after the call; records already taken are kept. */
+moe_status moe_profiler_filter(int32_t id);
 const char* moe_kernel_name(int32_t id);
 moe_status moe_profiler_read(int32_t id, int64_t* launches, double* total_ms);
 

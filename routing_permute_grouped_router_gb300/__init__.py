@@ -77,6 +77,7 @@ _SIGNATURES = {
     "moe_launch_count": [],
     "moe_profiler_enable": [_I],
     "moe_kernel_kinds": [],
+    "moe_profiler_filter": [ctypes.c_int32],
     "moe_kernel_name": [ctypes.c_int32],
     "moe_profiler_read": [ctypes.c_int32, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double)],
     "moe_status_string": [_I],
@@ -261,6 +262,15 @@ def moe_profiler_enable(on: bool) -> None:
     _check("moe_profiler_enable", lib().moe_profiler_enable(int(on)))
 
 
+def moe_profiler_filter(name: Optional[str]) -> None:
+    """Profile only the kernel kind called ``name`` (None: every kind)."""
+    idx = -1
+    if name is not None:
+        names = [lib().moe_kernel_name(i).decode() for i in range(lib().moe_kernel_kinds())]
+        idx = names.index(name)
+    _check("moe_profiler_filter", lib().moe_profiler_filter(idx))
+
+
 def moe_profiler_read() -> dict:
     """{kernel name: (launches, total ms)} for kernels launched while the profiler was on."""
     out = {}
@@ -283,7 +293,7 @@ def allocate_saved(cfg: MoeConfig, device="cuda") -> dict:
     """Caller-owned routing state and activations for ``moe_layer_fwd``/``moe_layer_bwd``."""
     import torch
 
-    R, T, k, E, d, f = moe_max_rows(cfg), cfg.T, cfg.k, cfg.E, cfg.d_model, cfg.d_ff
+    R, T, k, E, d, f = moe_max_rows(cfg), max(cfg.T, 1), cfg.k, cfg.E, cfg.d_model, cfg.d_ff
     i32, f32, act = torch.int32, torch.float32, _act_dtype(cfg)
     return dict(ids=torch.empty(T, k, dtype=i32, device=device), gates=torch.empty(T, k, dtype=f32, device=device),
                 slot=torch.empty(T, k, dtype=i32, device=device), row_of=torch.empty(T, k, dtype=i32, device=device),

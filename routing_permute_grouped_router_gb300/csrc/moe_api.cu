@@ -58,6 +58,7 @@ struct ProfRec {
 };
 std::mutex g_prof_mu;
 bool g_prof_on = false;
+int g_prof_filter = -1;
 std::vector<ProfRec> g_prof_recs;
 std::vector<cudaEvent_t> g_event_pool;
 thread_local int t_open_rec = -1;
@@ -76,14 +77,14 @@ cudaEvent_t pool_event() {
 const char* const kKernelNames[KK_COUNT] = {
     "router_topk",  "slot_scan",  "slot_assign",     "permute",      "gemm_up_swiglu", "gemm_down",
     "unpermute_combine", "combine_bwd", "gemm_dgrad_h_swiglu_bwd", "gemm_wgrad", "gemm_dgrad_x",
-    "transpose_wr", "dx_router",  "dwr_partial",     "dwr_reduce",   "zero", "split_wr"};
+    "transpose_wr", "dx_router",  "dwr",     "dwr_reduce",   "zero", "split_wr"};
 
 }  // namespace
 
 void launch_begin(int kind, cudaStream_t s) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
   std::lock_guard<std::mutex> lk(g_prof_mu);
-  if (!g_prof_on) {
+  if (!g_prof_on || (g_prof_filter >= 0 && g_prof_filter != kind)) {
     t_open_rec = -1;
     return;
   }
@@ -186,7 +187,7 @@ struct FwdScratch {
 };
 struct BwdScratch {
   void *dy_perm, *da, *db, *dx_perm;
-  float *dg, *dl, *W_rT, *partial;
+  float *dg, *dl, *W_rT;
 };
 
 RoutingScratch carve_routing(Carver& c, const Shape& s) {
@@ -224,7 +225,6 @@ BwdScratch carve_bwd(Carver& c, const Shape& s) {
   b.dg = static_cast<float*>(c.take((size_t)s.T * s.k * 4));
   b.dl = static_cast<float*>(c.take((size_t)s.T * s.E * 4));
   b.W_rT = static_cast<float*>(c.take((size_t)s.E * s.d * 4));
-  b.partial = static_cast<float*>(c.take((size_t)dwr_splits(s) * s.d * s.E * 4));
   return b;
 }
 size_t ws_bytes_for(const Shape& s, int training) {
@@ -283,7 +283,7 @@ moe_status do_dx_router(const Shape& s, const void* x, const void* dx_perm, cons
     return MOE_OK;
   }
   CUDA_TRY(launch_dx_router(s, dx_perm, row_of, dl, W_r, bs.W_rT, dx, err, st));
-  CUDA_TRY(launch_dwr(s, x, dl, bs.partial, dwr_splits(s), dW_r, accumulate, st));
+  CUDA_TRY(launch_dwr(s, x, dl, dW_r, accumulate, st));
   return MOE_OK;
 }
 
@@ -613,6 +613,13 @@ moe_status moe_profiler_enable(int on) {
 }
 
 int32_t moe_kernel_kinds(void) { return KK_COUNT; }
+
+moe_status moe_profiler_filter(int32_t id) {
+  if (id >= KK_COUNT) return MOE_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_filter = id < 0 ? -1 : id;
+  return MOE_OK;
+}
 
 const char* moe_kernel_name(int32_t id) {
   if (id < 0 || id >= KK_COUNT) return nullptr;

@@ -5,8 +5,11 @@
 //
 // All of them are HBM-bound row copies.  One warp owns one token row and moves
 // it in 16-byte vectors (8 bf16 or 4 fp32 per lane), so every warp access is a
-// contiguous 512-byte segment.  Sums run in fp32 in a fixed order (choice j
-// ascending), so results are deterministic and use no atomics.
+// contiguous 512-byte segment.  The kernels are templated on k so that each
+// lane issues all of a chunk's loads (8 vectors over the k rows) before it
+// uses any of them: one memory round trip per chunk instead of one per vector.
+// Sums run in fp32 in a fixed order (choice j ascending), so results are
+// deterministic and use no atomics.
 #include <float.h>
 
 #include "common.cuh"
@@ -15,25 +18,26 @@ namespace moe {
 namespace {
 
 constexpr int RW_WARPS = 8;  // warps (= token rows) per block
-constexpr int MAXK = 8;
+constexpr int INFLIGHT = 8;  // 16-byte loads each lane keeps in flight
 
 __device__ __forceinline__ bool row_ok(int64_t r, int64_t max_rows) { return r >= 0 && r < max_rows; }
 
-// -------------------------------------------------------------------------- //
-// Permute (scatter form: each token row is read once and written to each of
-// its kept rows); blocks past the token range zero the pad rows of one expert.
-// -------------------------------------------------------------------------- //
-struct PermArgs {
-  const char* x;
-  const int32_t* row_of;
-  const int32_t* counts;
-  const int32_t* offsets;
-  char* x_perm;
-  uint32_t* err;
-  int T, k, E, nvec;  // nvec = 16-byte vectors per row
-  int64_t max_rows;
-  int token_blocks;
-};
+// Row indices of token t's k assignments; out-of-range rows are reported and
+// treated as dropped.
+template <int K>
+__device__ __forceinline__ void load_rows(const int32_t* __restrict__ row_of, int t, int64_t max_rows, uint32_t* err,
+                                          int lane, uint32_t detail, int64_t (&rows)[K]) {
+#pragma unroll
+  for (int j = 0; j < K; ++j) {
+    const int64_t r = row_of[(size_t)t * K + j];
+    rows[j] = -1;
+    if (r >= 0 && !row_ok(r, max_rows)) {
+      if (lane == 0) report_error(err, DEV_BAD_ROW, detail);
+    } else {
+      rows[j] = r;
+    }
+  }
+}
 
 __device__ __forceinline__ void zero_pad_rows(const int32_t* counts, const int32_t* offsets, int e, char* buf,
                                               int nvec, int64_t max_rows, uint32_t* err, int warp, int lane,
@@ -48,6 +52,23 @@ __device__ __forceinline__ void zero_pad_rows(const int32_t* counts, const int32
     for (int v = lane; v < nvec; v += 32) stg16(buf + (r * nvec + v) * 16, z);
 }
 
+// -------------------------------------------------------------------------- //
+// Permute (scatter form: each token row is read once and written to each of
+// its kept rows); blocks past the token range zero the pad rows of one expert.
+// -------------------------------------------------------------------------- //
+struct PermArgs {
+  const char* x;
+  const int32_t* row_of;
+  const int32_t* counts;
+  const int32_t* offsets;
+  char* x_perm;
+  uint32_t* err;
+  int T, E, nvec;  // nvec = 16-byte vectors per row
+  int64_t max_rows;
+  int token_blocks;
+};
+
+template <int K>
 __global__ void __launch_bounds__(RW_WARPS * 32) permute_kernel(PermArgs a) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if ((int)blockIdx.x >= a.token_blocks) {
@@ -57,36 +78,24 @@ __global__ void __launch_bounds__(RW_WARPS * 32) permute_kernel(PermArgs a) {
   }
   const int t = blockIdx.x * RW_WARPS + warp;
   if (t >= a.T) return;
-  int64_t rows[MAXK];
+  int64_t rows[K];
+  load_rows<K>(a.row_of, t, a.max_rows, a.err, lane, 10, rows);
+  const char* __restrict__ src = a.x + (int64_t)t * a.nvec * 16;
+  char* __restrict__ dst = a.x_perm;
+  for (int v0 = 0; v0 < a.nvec; v0 += 32 * INFLIGHT) {
+    uint4 val[INFLIGHT];
 #pragma unroll
-  for (int j = 0; j < MAXK; ++j) {
-    rows[j] = -1;
-    if (j < a.k) {
-      const int64_t r = a.row_of[(size_t)t * a.k + j];
-      if (r >= 0 && !row_ok(r, a.max_rows)) {
-        if (lane == 0) report_error(a.err, DEV_BAD_ROW, 10);
-      } else {
-        rows[j] = r;
-      }
-    }
-  }
-  const char* src = a.x + (int64_t)t * a.nvec * 16;
-  constexpr int U = 4;
-  for (int v0 = lane; v0 < a.nvec; v0 += 32 * U) {
-    uint4 val[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int v = v0 + 32 * u;
+    for (int u = 0; u < INFLIGHT; ++u) {
+      const int v = v0 + lane + 32 * u;
       if (v < a.nvec) val[u] = ldg16(src + v * 16);
     }
 #pragma unroll
-    for (int j = 0; j < MAXK; ++j) {
+    for (int j = 0; j < K; ++j) {
       if (rows[j] < 0) continue;
-      char* dst = a.x_perm + rows[j] * a.nvec * 16;
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int v = v0 + 32 * u;
-        if (v < a.nvec) stg16(dst + v * 16, val[u]);
+      for (int u = 0; u < INFLIGHT; ++u) {
+        const int v = v0 + lane + 32 * u;
+        if (v < a.nvec) stg16(dst + (rows[j] * a.nvec + v) * 16, val[u]);
       }
     }
   }
@@ -101,46 +110,50 @@ struct CombArgs {
   const float* gates;
   char* y;
   uint32_t* err;
-  int T, k, nvec;
+  int T, nvec;
   int64_t max_rows;
 };
 
-template <typename Tx>
+template <typename Tx, int K>
 __global__ void __launch_bounds__(RW_WARPS * 32) combine_kernel(CombArgs a) {
   constexpr int VN = Vec<Tx>::N;
+  constexpr int U = INFLIGHT / K > 0 ? INFLIGHT / K : 1;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int t = blockIdx.x * RW_WARPS + warp;
   if (t >= a.T) return;
-  int64_t rows[MAXK];
-  float g[MAXK];
+  int64_t rows[K];
+  load_rows<K>(a.row_of, t, a.max_rows, a.err, lane, 11, rows);
+  float g[K];
 #pragma unroll
-  for (int j = 0; j < MAXK; ++j) {
-    rows[j] = -1;
-    g[j] = 0.f;
-    if (j < a.k) {
-      const int64_t r = a.row_of[(size_t)t * a.k + j];
-      if (r >= 0 && !row_ok(r, a.max_rows)) {
-        if (lane == 0) report_error(a.err, DEV_BAD_ROW, 11);
-      } else if (r >= 0) {
-        rows[j] = r;
-        g[j] = a.gates[(size_t)t * a.k + j];
+  for (int j = 0; j < K; ++j) g[j] = rows[j] >= 0 ? a.gates[(size_t)t * K + j] : 0.f;
+  const char* __restrict__ yp = a.y_perm;
+  char* __restrict__ dst = a.y + (int64_t)t * a.nvec * 16;
+  for (int v0 = 0; v0 < a.nvec; v0 += 32 * U) {
+    uint4 buf[K][U];
+#pragma unroll
+    for (int j = 0; j < K; ++j)
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + lane + 32 * u;
+        buf[j][u] = (rows[j] >= 0 && v < a.nvec) ? ldg16(yp + (rows[j] * a.nvec + v) * 16) : make_uint4(0, 0, 0, 0);
       }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + lane + 32 * u;
+      if (v >= a.nvec) continue;
+      float acc[VN];
+#pragma unroll
+      for (int i = 0; i < VN; ++i) acc[i] = 0.f;
+#pragma unroll
+      for (int j = 0; j < K; ++j) {
+        if (rows[j] < 0) continue;
+        float val[VN];
+        unpack(buf[j][u], val);
+#pragma unroll
+        for (int i = 0; i < VN; ++i) acc[i] = fmaf(g[j], val[i], acc[i]);
+      }
+      stg16(dst + v * 16, pack(acc));
     }
-  }
-  char* dst = a.y + (int64_t)t * a.nvec * 16;
-  for (int v = lane; v < a.nvec; v += 32) {
-    float acc[VN];
-#pragma unroll
-    for (int i = 0; i < VN; ++i) acc[i] = 0.f;
-#pragma unroll
-    for (int j = 0; j < MAXK; ++j) {
-      if (rows[j] < 0) continue;
-      float val[VN];
-      unpack(ldg16(a.y_perm + (rows[j] * a.nvec + v) * 16), val);
-#pragma unroll
-      for (int i = 0; i < VN; ++i) acc[i] = fmaf(g[j], val[i], acc[i]);
-    }
-    stg16(dst + v * 16, pack(acc));
   }
 }
 
@@ -161,14 +174,15 @@ struct CombBwdArgs {
   float* dg;
   float* dl;
   uint32_t* err;
-  int T, k, E, nvec;
+  int T, E, nvec;
   int64_t max_rows;
   int token_blocks;
 };
 
-template <typename Tx>
+template <typename Tx, int K>
 __global__ void __launch_bounds__(RW_WARPS * 32) combine_bwd_kernel(CombBwdArgs a) {
   constexpr int VN = Vec<Tx>::N;
+  constexpr int U = INFLIGHT / (K + 1) > 0 ? INFLIGHT / (K + 1) : 1;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if ((int)blockIdx.x >= a.token_blocks) {
     zero_pad_rows(a.counts, a.offsets, blockIdx.x - a.token_blocks, a.dy_perm, a.nvec, a.max_rows, a.err, warp,
@@ -177,53 +191,66 @@ __global__ void __launch_bounds__(RW_WARPS * 32) combine_bwd_kernel(CombBwdArgs 
   }
   const int t = blockIdx.x * RW_WARPS + warp;
   if (t >= a.T) return;
-  int64_t rows[MAXK];
-  float g[MAXK], part[MAXK];
+  int64_t rows[K];
+  load_rows<K>(a.row_of, t, a.max_rows, a.err, lane, 12, rows);
+  float g[K], part[K];
 #pragma unroll
-  for (int j = 0; j < MAXK; ++j) {
-    rows[j] = -1;
-    g[j] = 0.f;
+  for (int j = 0; j < K; ++j) {
+    g[j] = a.gates[(size_t)t * K + j];
     part[j] = 0.f;
-    if (j < a.k) {
-      g[j] = a.gates[(size_t)t * a.k + j];
-      const int64_t r = a.row_of[(size_t)t * a.k + j];
-      if (r >= 0 && !row_ok(r, a.max_rows)) {
-        if (lane == 0) report_error(a.err, DEV_BAD_ROW, 12);
-      } else {
-        rows[j] = r;
+  }
+  const char* __restrict__ src = a.dy + (int64_t)t * a.nvec * 16;
+  const char* __restrict__ yp = a.y_perm;
+  char* __restrict__ out = a.dy_perm;
+  for (int v0 = 0; v0 < a.nvec; v0 += 32 * U) {
+    uint4 dyb[U], yb[K][U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + lane + 32 * u;
+      dyb[u] = v < a.nvec ? ldg16(src + v * 16) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < K; ++j)
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + lane + 32 * u;
+        yb[j][u] = (rows[j] >= 0 && v < a.nvec) ? ldg16(yp + (rows[j] * a.nvec + v) * 16) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + lane + 32 * u;
+      if (v >= a.nvec) continue;
+      float dyv[VN];
+      unpack(dyb[u], dyv);
+#pragma unroll
+      for (int j = 0; j < K; ++j) {
+        if (rows[j] < 0) continue;
+        float yv[VN], o[VN];
+        unpack(yb[j][u], yv);
+#pragma unroll
+        for (int i = 0; i < VN; ++i) {
+          part[j] = fmaf(dyv[i], yv[i], part[j]);
+          o[i] = g[j] * dyv[i];
+        }
+        stg16(out + (rows[j] * a.nvec + v) * 16, pack(o));
       }
     }
   }
-  const char* src = a.dy + (int64_t)t * a.nvec * 16;
-  for (int v = lane; v < a.nvec; v += 32) {
-    float dyv[VN];
-    unpack(ldg16(src + v * 16), dyv);
-#pragma unroll
-    for (int j = 0; j < MAXK; ++j) {
-      if (rows[j] < 0) continue;
-      float yv[VN], o[VN];
-      unpack(ldg16(a.y_perm + (rows[j] * a.nvec + v) * 16), yv);
-#pragma unroll
-      for (int i = 0; i < VN; ++i) {
-        part[j] = fmaf(dyv[i], yv[i], part[j]);
-        o[i] = g[j] * dyv[i];
-      }
-      stg16(a.dy_perm + (rows[j] * a.nvec + v) * 16, pack(o));
-    }
-  }
-  float dg[MAXK];
+  float dg[K];
   float s = 0.f;
 #pragma unroll
-  for (int j = 0; j < MAXK; ++j) {
-    dg[j] = (j < a.k) ? warp_sum(part[j]) : 0.f;
+  for (int j = 0; j < K; ++j) {
+    dg[j] = warp_sum(part[j]);
     s = fmaf(g[j], dg[j], s);
   }
-  if (lane == 0) {
+  if (lane < K) {
+    float mine = 0.f;
 #pragma unroll
-    for (int j = 0; j < MAXK; ++j)
-      if (j < a.k) a.dg[(size_t)t * a.k + j] = dg[j];
+    for (int j = 0; j < K; ++j)
+      if (lane == j) mine = dg[j];
+    a.dg[(size_t)t * K + lane] = mine;
   }
-  if (a.k == 1) {
+  if (K == 1) {
     const int e1 = a.ids[(size_t)t];
     const float gd = g[0] * dg[0];
     for (int e = lane; e < a.E; e += 32) {
@@ -231,11 +258,14 @@ __global__ void __launch_bounds__(RW_WARPS * 32) combine_bwd_kernel(CombBwdArgs 
       a.dl[(size_t)t * a.E + e] = gd * ((e == e1 ? 1.f : 0.f) - p);
     }
   } else {
+    int ids[K];
+#pragma unroll
+    for (int j = 0; j < K; ++j) ids[j] = a.ids[(size_t)t * K + j];
     for (int e = lane; e < a.E; e += 32) {
       float v = 0.f;
 #pragma unroll
-      for (int j = 0; j < MAXK; ++j)
-        if (j < a.k && a.ids[(size_t)t * a.k + j] == e) v += g[j] * (dg[j] - s);
+      for (int j = 0; j < K; ++j)
+        if (ids[j] == e) v += g[j] * (dg[j] - s);
       a.dl[(size_t)t * a.E + e] = v;
     }
   }
@@ -268,29 +298,19 @@ struct DxArgs {
   const float* W_rT;
   char* dx;
   uint32_t* err;
-  int T, k, E, d, nvec;
+  int T, E, d, nvec;
   int64_t max_rows;
 };
 
-template <typename Tx>
+template <typename Tx, int K>
 __global__ void __launch_bounds__(RW_WARPS * 32) dx_router_kernel(DxArgs a) {
   constexpr int VN = Vec<Tx>::N;
+  constexpr int U = INFLIGHT / K > 0 ? INFLIGHT / K : 1;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int t = blockIdx.x * RW_WARPS + warp;
   if (t >= a.T) return;
-  int64_t rows[MAXK];
-#pragma unroll
-  for (int j = 0; j < MAXK; ++j) {
-    rows[j] = -1;
-    if (j < a.k) {
-      const int64_t r = a.row_of[(size_t)t * a.k + j];
-      if (r >= 0 && !row_ok(r, a.max_rows)) {
-        if (lane == 0) report_error(a.err, DEV_BAD_ROW, 13);
-      } else {
-        rows[j] = r;
-      }
-    }
-  }
+  int64_t rows[K];
+  load_rows<K>(a.row_of, t, a.max_rows, a.err, lane, 13, rows);
   // Experts with a nonzero logit gradient (at most k of them when k > 1),
   // found with all lanes active before the row loop.
   const float* dlt = a.dl + (size_t)t * a.E;
@@ -301,139 +321,200 @@ __global__ void __launch_bounds__(RW_WARPS * 32) dx_router_kernel(DxArgs a) {
     const float mine = (e < a.E) ? dlt[e] : 0.f;
     nzmask[c] = __ballot_sync(0xffffffffu, mine != 0.f);
   }
-  for (int v = lane; v < a.nvec; v += 32) {
-    float acc[VN];
+  const char* __restrict__ xp = a.dx_perm;
+  char* __restrict__ dst = a.dx + (int64_t)t * a.nvec * 16;
+  for (int v0 = 0; v0 < a.nvec; v0 += 32 * U) {
+    uint4 buf[K][U];
 #pragma unroll
-    for (int i = 0; i < VN; ++i) acc[i] = 0.f;
+    for (int j = 0; j < K; ++j)
 #pragma unroll
-    for (int j = 0; j < MAXK; ++j) {
-      if (rows[j] < 0) continue;
-      float val[VN];
-      unpack(ldg16(a.dx_perm + (rows[j] * a.nvec + v) * 16), val);
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + lane + 32 * u;
+        buf[j][u] = (rows[j] >= 0 && v < a.nvec) ? ldg16(xp + (rows[j] * a.nvec + v) * 16) : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
-      for (int i = 0; i < VN; ++i) acc[i] += val[i];
-    }
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + lane + 32 * u;
+      if (v >= a.nvec) continue;
+      float acc[VN];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      unsigned nz = nzmask[c];
-      while (nz) {
-        const int e = 32 * c + __ffs(nz) - 1;
-        nz &= nz - 1;
-        const float w = dlt[e];
-        const float4* wr = reinterpret_cast<const float4*>(a.W_rT + (size_t)e * a.d + (size_t)v * VN);
+      for (int i = 0; i < VN; ++i) acc[i] = 0.f;
 #pragma unroll
-        for (int q = 0; q < VN / 4; ++q) {
-          const float4 w4 = wr[q];
-          acc[4 * q + 0] = fmaf(w, w4.x, acc[4 * q + 0]);
-          acc[4 * q + 1] = fmaf(w, w4.y, acc[4 * q + 1]);
-          acc[4 * q + 2] = fmaf(w, w4.z, acc[4 * q + 2]);
-          acc[4 * q + 3] = fmaf(w, w4.w, acc[4 * q + 3]);
+      for (int j = 0; j < K; ++j) {
+        if (rows[j] < 0) continue;
+        float val[VN];
+        unpack(buf[j][u], val);
+#pragma unroll
+        for (int i = 0; i < VN; ++i) acc[i] += val[i];
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        unsigned nz = nzmask[c];
+        while (nz) {
+          const int e = 32 * c + __ffs(nz) - 1;
+          nz &= nz - 1;
+          const float w = dlt[e];
+          const float4* wr = reinterpret_cast<const float4*>(a.W_rT + (size_t)e * a.d + (size_t)v * VN);
+#pragma unroll
+          for (int qq = 0; qq < VN / 4; ++qq) {
+            const float4 w4 = wr[qq];
+            acc[4 * qq + 0] = fmaf(w, w4.x, acc[4 * qq + 0]);
+            acc[4 * qq + 1] = fmaf(w, w4.y, acc[4 * qq + 1]);
+            acc[4 * qq + 2] = fmaf(w, w4.z, acc[4 * qq + 2]);
+            acc[4 * qq + 3] = fmaf(w, w4.w, acc[4 * qq + 3]);
+          }
         }
       }
+      stg16(dst + v * 16, pack(acc));
     }
-    stg16(a.dx + ((int64_t)t * a.nvec + v) * 16, pack(acc));
   }
 }
 
 // -------------------------------------------------------------------------- //
-// dW_r = x^T dl: partial sums over token splits, then a fixed-order reduction.
+// dW_r (+)= x^T dl in one pass.  A block owns 8 columns of x and 8 experts; its
+// 256 threads take the tokens round-robin, each accumulating an 8x8 fp32 tile,
+// then the block reduces the tiles in a fixed order (warp shuffles, then the
+// eight warps in index order): deterministic, no atomics, no second kernel.
 // -------------------------------------------------------------------------- //
-constexpr int DW_COLS = 64;
-constexpr int DW_TOK = 32;
+constexpr int DW_THREADS = 256;
 
 struct DwArgs {
   const void* x;
   const float* dl;
-  float* partial;  // [splits, d, E]
-  int T, d, E, tok_per_split;
+  float* dW_r;
+  int T, d, E, accumulate;
 };
 
-template <int EP, typename Tx>
-__global__ void __launch_bounds__(256) dwr_partial_kernel(DwArgs a) {
-  constexpr int EQ = EP / 4;  // experts per thread
-  __shared__ float dls[DW_TOK][EP];
-  __shared__ float xs[DW_TOK][DW_COLS + 1];
+template <typename Tx>
+__global__ void __launch_bounds__(DW_THREADS) dwr_kernel(DwArgs a) {
+  __shared__ float part[DW_THREADS / 32][64];
+  const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+  const int e0 = blockIdx.x * 8, i0 = blockIdx.y * 8;  // experts fastest: neighbours share x columns
   const Tx* x = static_cast<const Tx*>(a.x);
-  const int tid = threadIdx.x, col = tid % DW_COLS, eg = tid / DW_COLS;
-  const int i0 = blockIdx.x * DW_COLS, s = blockIdx.y;
-  const int tb = s * a.tok_per_split, te = min(a.T, tb + a.tok_per_split);
-  float acc[EQ];
+  const bool full_e = e0 + 8 <= a.E && (a.E % 4) == 0;
+  const bool full_i = i0 + 8 <= a.d;
+  float acc[8][8];
 #pragma unroll
-  for (int q = 0; q < EQ; ++q) acc[q] = 0.f;
-  for (int t0 = tb; t0 < te; t0 += DW_TOK) {
-    for (int idx = tid; idx < DW_TOK * EP; idx += 256) {
-      const int r = idx / EP, e = idx % EP, t = t0 + r;
-      dls[r][e] = (t < te && e < a.E) ? a.dl[(size_t)t * a.E + e] : 0.f;
-    }
-    for (int idx = tid; idx < DW_TOK * DW_COLS; idx += 256) {
-      const int r = idx / DW_COLS, c = idx % DW_COLS, t = t0 + r, i = i0 + c;
-      xs[r][c] = (t < te && i < a.d) ? to_f32(x[(size_t)t * a.d + i]) : 0.f;
-    }
-    __syncthreads();
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
 #pragma unroll 4
-    for (int r = 0; r < DW_TOK; ++r) {
-      const float xv = xs[r][col];
+  for (int t = tid; t < a.T; t += DW_THREADS) {
+    float xv[8], lv[8];
+    if (full_i) {
+      const Tx* xr = x + (size_t)t * a.d + i0;
+      if (sizeof(Tx) == 2) {
+        unpack(*reinterpret_cast<const uint4*>(xr), xv);
+      } else {
+        const float4 p0 = reinterpret_cast<const float4*>(xr)[0], p1 = reinterpret_cast<const float4*>(xr)[1];
+        xv[0] = p0.x; xv[1] = p0.y; xv[2] = p0.z; xv[3] = p0.w;
+        xv[4] = p1.x; xv[5] = p1.y; xv[6] = p1.z; xv[7] = p1.w;
+      }
+    } else {
 #pragma unroll
-      for (int q = 0; q < EQ; ++q) acc[q] = fmaf(xv, dls[r][eg + 4 * q], acc[q]);
+      for (int i = 0; i < 8; ++i) xv[i] = (i0 + i < a.d) ? to_f32(x[(size_t)t * a.d + i0 + i]) : 0.f;
     }
-    __syncthreads();
-  }
-  const int i = i0 + col;
-  if (i < a.d) {
+    const float* lr = a.dl + (size_t)t * a.E + e0;
+    if (full_e) {
+      const float4 q0 = reinterpret_cast<const float4*>(lr)[0], q1 = reinterpret_cast<const float4*>(lr)[1];
+      lv[0] = q0.x; lv[1] = q0.y; lv[2] = q0.z; lv[3] = q0.w;
+      lv[4] = q1.x; lv[5] = q1.y; lv[6] = q1.z; lv[7] = q1.w;
+    } else {
 #pragma unroll
-    for (int q = 0; q < EQ; ++q) {
-      const int e = eg + 4 * q;
-      if (e < a.E) a.partial[((size_t)s * a.d + i) * a.E + e] = acc[q];
+      for (int e = 0; e < 8; ++e) lv[e] = (e0 + e < a.E) ? lr[e] : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(xv[i], lv[e], acc[i][e]);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float v = warp_sum(acc[i][e]);
+      if (lane == 0) part[warp][i * 8 + e] = v;
+    }
+  __syncthreads();
+  if (tid < 64) {
+    const int i = i0 + tid / 8, e = e0 + tid % 8;
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < DW_THREADS / 32; ++w) s += part[w][tid];
+    if (i < a.d && e < a.E) {
+      float* o = a.dW_r + (size_t)i * a.E + e;
+      *o = a.accumulate ? *o + s : s;
     }
   }
-}
-
-__global__ void dwr_reduce_kernel(const float* partial, float* dW_r, int splits, int64_t n, int accumulate) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n) return;
-  float s = accumulate ? dW_r[i] : 0.f;
-  float p = 0.f;
-  for (int q = 0; q < splits; ++q) p += partial[(size_t)q * n + i];
-  dW_r[i] = s + p;
-}
-
-template <int EP>
-cudaError_t launch_dwr_ep(const Shape& s, const DwArgs& a, int splits, cudaStream_t st) {
-  dim3 grid((s.d + DW_COLS - 1) / DW_COLS, splits);
-  LaunchScope ls(KK_DWR_PARTIAL, st);
-  if (s.bf16)
-    dwr_partial_kernel<EP, __nv_bfloat16><<<grid, 256, 0, st>>>(a);
-  else
-    dwr_partial_kernel<EP, float><<<grid, 256, 0, st>>>(a);
-  return cudaGetLastError();
 }
 
 int row_vecs(const Shape& s) { return s.d * (s.bf16 ? 2 : 4) / 16; }
+
+// Dispatch a (dtype, k) templated row kernel; k ranges over 1..8.
+template <template <typename, int> class Kern, typename Args>
+cudaError_t launch_typed_k(const Shape& s, const Args& a, int grid, cudaStream_t st) {
+#define MOE_ROWS_CASE(KK)                                    \
+  case KK:                                                   \
+    if (s.bf16) Kern<__nv_bfloat16, KK>::launch(a, grid, st); \
+    else Kern<float, KK>::launch(a, grid, st);               \
+    break;
+  switch (s.k) {
+    MOE_ROWS_CASE(1)
+    MOE_ROWS_CASE(2)
+    MOE_ROWS_CASE(3)
+    MOE_ROWS_CASE(4)
+    MOE_ROWS_CASE(5)
+    MOE_ROWS_CASE(6)
+    MOE_ROWS_CASE(7)
+    MOE_ROWS_CASE(8)
+    default: return cudaErrorInvalidValue;
+  }
+#undef MOE_ROWS_CASE
+  return cudaGetLastError();
+}
+
+template <typename Tx, int K>
+struct CombineL {
+  static void launch(const CombArgs& a, int grid, cudaStream_t st) {
+    combine_kernel<Tx, K><<<grid, RW_WARPS * 32, 0, st>>>(a);
+  }
+};
+template <typename Tx, int K>
+struct CombineBwdL {
+  static void launch(const CombBwdArgs& a, int grid, cudaStream_t st) {
+    combine_bwd_kernel<Tx, K><<<grid, RW_WARPS * 32, 0, st>>>(a);
+  }
+};
+template <typename Tx, int K>
+struct DxL {
+  static void launch(const DxArgs& a, int grid, cudaStream_t st) {
+    dx_router_kernel<Tx, K><<<grid, RW_WARPS * 32, 0, st>>>(a);
+  }
+};
+template <typename Tx, int K>
+struct PermuteL {  // byte copies: the element type does not matter
+  static void launch(const PermArgs& a, int grid, cudaStream_t st) {
+    permute_kernel<K><<<grid, RW_WARPS * 32, 0, st>>>(a);
+  }
+};
 
 }  // namespace
 
 cudaError_t launch_permute(const Shape& s, const void* x, const int32_t* row_of, const int32_t* counts,
                            const int32_t* offsets, void* x_perm, uint32_t* err, cudaStream_t st) {
   PermArgs a{static_cast<const char*>(x), row_of, counts, offsets, static_cast<char*>(x_perm), err,
-             s.T, s.k, s.E, row_vecs(s), s.max_rows, (s.T + RW_WARPS - 1) / RW_WARPS};
-  const int grid = a.token_blocks + s.E;
+             s.T, s.E, row_vecs(s), s.max_rows, (s.T + RW_WARPS - 1) / RW_WARPS};
   LaunchScope ls(KK_PERMUTE, st);
-  permute_kernel<<<grid, RW_WARPS * 32, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_typed_k<PermuteL>(s, a, a.token_blocks + s.E, st);
 }
 
 cudaError_t launch_combine(const Shape& s, const void* y_perm, const int32_t* row_of, const float* gates, void* y,
                            uint32_t* err, cudaStream_t st) {
   if (s.T == 0) return cudaSuccess;
-  CombArgs a{static_cast<const char*>(y_perm), row_of, gates, static_cast<char*>(y), err, s.T, s.k, row_vecs(s),
+  CombArgs a{static_cast<const char*>(y_perm), row_of, gates, static_cast<char*>(y), err, s.T, row_vecs(s),
              s.max_rows};
-  const int grid = (s.T + RW_WARPS - 1) / RW_WARPS;
   LaunchScope ls(KK_COMBINE, st);
-  if (s.bf16)
-    combine_kernel<__nv_bfloat16><<<grid, RW_WARPS * 32, 0, st>>>(a);
-  else
-    combine_kernel<float><<<grid, RW_WARPS * 32, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_typed_k<CombineL>(s, a, (s.T + RW_WARPS - 1) / RW_WARPS, st);
 }
 
 cudaError_t launch_combine_bwd(const Shape& s, const void* dy, const void* y_perm, const int32_t* ids,
@@ -441,15 +522,10 @@ cudaError_t launch_combine_bwd(const Shape& s, const void* dy, const void* y_per
                                const int32_t* counts, const int32_t* offsets, void* dy_perm, float* dg, float* dl,
                                uint32_t* err, cudaStream_t st) {
   CombBwdArgs a{static_cast<const char*>(dy), static_cast<const char*>(y_perm), ids, row_of, gates, probs,
-                counts, offsets, static_cast<char*>(dy_perm), dg, dl, err, s.T, s.k, s.E, row_vecs(s), s.max_rows,
+                counts, offsets, static_cast<char*>(dy_perm), dg, dl, err, s.T, s.E, row_vecs(s), s.max_rows,
                 (s.T + RW_WARPS - 1) / RW_WARPS};
-  const int grid = a.token_blocks + s.E;
   LaunchScope ls(KK_COMBINE_BWD, st);
-  if (s.bf16)
-    combine_bwd_kernel<__nv_bfloat16><<<grid, RW_WARPS * 32, 0, st>>>(a);
-  else
-    combine_bwd_kernel<float><<<grid, RW_WARPS * 32, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_typed_k<CombineBwdL>(s, a, a.token_blocks + s.E, st);
 }
 
 cudaError_t launch_dx_router(const Shape& s, const void* dx_perm, const int32_t* row_of, const float* dl,
@@ -462,41 +538,19 @@ cudaError_t launch_dx_router(const Shape& s, const void* dx_perm, const int32_t*
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  DxArgs a{static_cast<const char*>(dx_perm), row_of, dl, W_rT, static_cast<char*>(dx), err, s.T, s.k, s.E, s.d,
+  DxArgs a{static_cast<const char*>(dx_perm), row_of, dl, W_rT, static_cast<char*>(dx), err, s.T, s.E, s.d,
            row_vecs(s), s.max_rows};
-  const int grid = (s.T + RW_WARPS - 1) / RW_WARPS;
   LaunchScope ls(KK_DX_ROUTER, st);
-  if (s.bf16)
-    dx_router_kernel<__nv_bfloat16><<<grid, RW_WARPS * 32, 0, st>>>(a);
-  else
-    dx_router_kernel<float><<<grid, RW_WARPS * 32, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_typed_k<DxL>(s, a, (s.T + RW_WARPS - 1) / RW_WARPS, st);
 }
 
-int dwr_splits(const Shape& s) {
-  const int col_blocks = (s.d + DW_COLS - 1) / DW_COLS;
-  int splits = (2 * 152 + col_blocks - 1) / col_blocks;
-  const int max_splits = (s.T + DW_TOK - 1) / DW_TOK;
-  if (splits > max_splits) splits = max_splits;
-  if (splits < 1) splits = 1;
-  return splits;
-}
-
-cudaError_t launch_dwr(const Shape& s, const void* x, const float* dl, float* partial, int splits, float* dW_r,
-                       int accumulate, cudaStream_t st) {
-  int tps = (s.T + splits - 1) / splits;
-  tps = (tps + DW_TOK - 1) / DW_TOK * DW_TOK;
-  DwArgs a{x, dl, partial, s.T, s.d, s.E, tps};
-  cudaError_t e;
-  if (s.E <= 8) e = launch_dwr_ep<8>(s, a, splits, st);
-  else if (s.E <= 16) e = launch_dwr_ep<16>(s, a, splits, st);
-  else if (s.E <= 32) e = launch_dwr_ep<32>(s, a, splits, st);
-  else if (s.E <= 64) e = launch_dwr_ep<64>(s, a, splits, st);
-  else e = launch_dwr_ep<128>(s, a, splits, st);
-  if (e != cudaSuccess) return e;
-  const int64_t n = (int64_t)s.d * s.E;
-  LaunchScope ls(KK_DWR_REDUCE, st);
-  dwr_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(partial, dW_r, splits, n, accumulate);
+cudaError_t launch_dwr(const Shape& s, const void* x, const float* dl, float* dW_r, int accumulate,
+                       cudaStream_t st) {
+  DwArgs a{x, dl, dW_r, s.T, s.d, s.E, accumulate};
+  dim3 grid((s.E + 7) / 8, (s.d + 7) / 8);
+  LaunchScope ls(KK_DWR, st);
+  if (s.bf16) dwr_kernel<__nv_bfloat16><<<grid, DW_THREADS, 0, st>>>(a);
+  else dwr_kernel<float><<<grid, DW_THREADS, 0, st>>>(a);
   return cudaGetLastError();
 }
 

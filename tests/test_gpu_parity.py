@@ -184,6 +184,28 @@ def test_edge_cases(shape):
         assert (L.saved["gates"].cpu() == 1.0).all()
 
 
+@pytest.mark.parametrize("cf", [1.25, 0.0])
+def test_zero_tokens(cf):
+    """T = 0: no work, zero gradients when overwriting, untouched when accumulating."""
+    s = LS("empty", 0, 256, 256, 4, 2, cf, W.BF16, backward=True)
+    wl = W.make(s.replace(T=8), micro_batches=1, with_dy=True)
+    L = layer.from_workload(wl, T=0)
+    x = torch.zeros(1, s.d_model, dtype=torch.bfloat16, device="cuda")  # a valid pointer; no row is read
+    for n in L.grads:
+        L.grads[n].fill_(3.0)
+    L.forward(x)
+    L.backward(x, x, accumulate=True)
+    torch.cuda.synchronize()
+    check_no_device_error()
+    for n in L.grads:
+        assert (L.grads[n] == 3.0).all(), n
+    L.backward(x, x, accumulate=False)
+    torch.cuda.synchronize()
+    for n in L.grads:
+        assert not L.grads[n].any(), n
+    assert not L.saved["counts"].any() and not L.saved["offsets"].any()
+
+
 def test_huge_capacity_equals_dropless_bitwise():
     a = LS("huge", 500, 256, 256, 6, 2, 0.0, W.BF16, capacity=10 ** 6)
     b = a.replace(capacity=-1, capacity_factor=0.0)
