@@ -130,6 +130,16 @@ __device__ __forceinline__ void box_put_f32x32(uint32_t box, int lane, const flo
     sts128(box_chunk(box, lane, q), make_uint4(__float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]),
                                                __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3])));
 }
+__device__ __forceinline__ void box_get_f32x32(uint32_t box, int lane, float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const uint4 u = lds128(box_chunk(box, lane, q));
+    v[4 * q] = __uint_as_float(u.x);
+    v[4 * q + 1] = __uint_as_float(u.y);
+    v[4 * q + 2] = __uint_as_float(u.z);
+    v[4 * q + 3] = __uint_as_float(u.w);
+  }
+}
 __device__ __forceinline__ void regs_to_f32(const uint32_t (&r)[32], float (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
@@ -273,6 +283,23 @@ __device__ __forceinline__ bool epilogue_tile(const TcMaps& maps, const TcArgs& 
     es.pending[h] = true;
     __syncwarp();
   }
+  // wgrad accumulating into the fp32 gradient: fetch the first box of old
+  // values while the mainloop still runs (read, add and store back below)
+  const bool wg_add = MODE == M_WGRAD && a.accumulate && t.kblocks > 0;
+  const int wg_rows = MODE == M_WGRAD ? (t.sub == 2 ? a.f : a.d) : 0;
+  const CUtensorMap* wg_map = &maps.m[MODE == M_WGRAD ? 5 + t.sub : 0];
+  const int wg_orow = t.e * wg_rows + t.m0 + q * 32;
+  if (wg_add) {
+    const uint32_t h = es.nbox & 1;
+    if (lane == 0) {
+      bulk_wait_read0();
+      const uint32_t bar = lbar + 8 * h;
+      mbar_expect_tx(bar, BOX_BYTES);
+      tma_load_2d(ebuf + h * BOX_BYTES, wg_map, bar, t.n0, wg_orow);
+    }
+    es.pending[h] = true;
+    __syncwarp();
+  }
   if (!mbar_wait(tfull, tfull_parity, abort_flag, a.err, 400 + MODE)) return false;
   tc_fence_after();
 
@@ -382,11 +409,37 @@ __device__ __forceinline__ bool epilogue_tile(const TcMaps& maps, const TcArgs& 
       }
     }
     es.nbox += 4;
-  } else {  // WGRAD: fp32 weight-gradient rows, stored or added in place
+  } else if (wg_add) {  // WGRAD, accumulate: dW += acc via TMA load, add, TMA store
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+      const uint32_t h = (es.nbox + c) & 1;
+      const uint32_t buf = ebuf + h * BOX_BYTES;
+      if (c + 1 < 8) {
+        const uint32_t hn = h ^ 1u;
+        if (lane == 0) {
+          bulk_wait_read0();  // the store that last used buffer hn has read it
+          const uint32_t bar = lbar + 8 * hn;
+          mbar_expect_tx(bar, BOX_BYTES);
+          tma_load_2d(ebuf + hn * BOX_BYTES, wg_map, bar, t.n0 + (c + 1) * 32, wg_orow);
+        }
+        es.pending[hn] = true;
+      }
+      uint32_t r[32];
+      tmem_ld32(tacc + c * 32, r);
+      tmem_ld_wait(r);
+      if (!mbar_wait(lbar + 8 * h, es.uses[h] & 1u, abort_flag, a.err, 501)) return false;
+      ++es.uses[h];
+      es.pending[h] = false;
+      float old[32], v[32];
+      box_get_f32x32(buf, lane, old);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = old[i] + __uint_as_float(r[i]);
+      box_put_f32x32(buf, lane, v);
+      box_issue_store(wg_map, buf, t.n0 + c * 32, wg_orow, lane);
+    }
+    es.nbox += 8;
+  } else {  // WGRAD, overwrite (or an expert with no rows and accumulate = 0)
     if (t.kblocks == 0 && a.accumulate) return true;
-    const int M = t.sub == 2 ? a.f : a.d;
-    const CUtensorMap* om = &maps.m[5 + t.sub];
-    const int orow = t.e * M + t.m0 + q * 32;
 #pragma unroll 1
     for (int c = 0; c < 8; ++c) {
       const uint32_t buf = ebuf + (es.nbox & 1) * BOX_BYTES;
@@ -402,13 +455,7 @@ __device__ __forceinline__ bool epilogue_tile(const TcMaps& maps, const TcArgs& 
         for (int i = 0; i < 32; ++i) v[i] = 0.f;
       }
       box_put_f32x32(buf, lane, v);
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        if (a.accumulate) tma_reduce_add_2d(om, buf, t.n0 + c * 32, orow);
-        else tma_store_2d(om, buf, t.n0 + c * 32, orow);
-        bulk_commit();
-      }
+      box_issue_store(wg_map, buf, t.n0 + c * 32, wg_orow, lane);
       ++es.nbox;
     }
   }
