@@ -144,22 +144,37 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- #
 # algorithmic work per kernel (per launch)
 # ----------------------------------------------------------------------------- #
-def algorithmic_work(s, N: int):
-    """(unit, amount) per launch: FLOPs for the GEMMs, bytes for the row moves."""
+def algorithmic_work(s, N: int, accumulate: bool = True):
+    """(FLOPs, bytes) per launch of each kernel: the work the layer defines, counted on the N kept
+    assignments (pad rows excluded); bytes are each operand read once and each result written once."""
     T, d, f, E, k = s.T, s.d_model, s.d_ff, s.E, s.k
     es = 2 if s.dtype == "bf16" else 4
+    Wb = E * d * f * es  # one expert weight tensor
+    grad_rw = 3 * E * d * f * 4 * (2 if accumulate else 1)
     return {
-        "router_topk": ("bytes", T * d * es + d * E * 4 + T * k * 8 + T * E * 4),
-        "permute": ("bytes", T * d * es + N * d * es),
-        "gemm_up_swiglu": ("flops", 4 * N * d * f),
-        "gemm_down": ("flops", 2 * N * f * d),
-        "unpermute_combine": ("bytes", N * d * es + T * d * es),
-        "combine_bwd": ("bytes", T * d * es + 2 * N * d * es + T * E * 4),
-        "gemm_dgrad_h_swiglu_bwd": ("flops", 2 * N * d * f),
-        "gemm_wgrad": ("flops", 6 * N * d * f),
-        "gemm_dgrad_x": ("flops", 4 * N * f * d),
-        "dx_router": ("bytes", N * d * es + T * d * es),
+        "router_topk": (2 * T * d * E, T * d * es + d * E * 4 + T * k * 8 + T * E * 4),
+        "permute": (0, T * d * es + N * d * es),
+        "gemm_up_swiglu": (4 * N * d * f, N * d * es + 2 * Wb + 3 * N * f * es),
+        "gemm_down": (2 * N * f * d, N * f * es + Wb + N * d * es),
+        "unpermute_combine": (0, N * d * es + T * d * es),
+        "combine_bwd": (0, T * d * es + 2 * N * d * es + T * E * 4),
+        "gemm_dgrad_h_swiglu_bwd": (2 * N * d * f, N * d * es + Wb + 4 * N * f * es),
+        "gemm_wgrad": (6 * N * d * f, 2 * N * d * es + 3 * N * f * es + grad_rw),
+        "gemm_dgrad_x": (4 * N * f * d, 2 * N * f * es + 2 * Wb + N * d * es),
+        "dx_router": (0, N * d * es + T * d * es),
     }
+
+
+def binding(flops: float, nbytes: float, seconds: float, tflops_peak: float, hbm_peak: float) -> dict:
+    """The roofline that binds a launch: tensor if its ideal FLOP time is the longer, else HBM."""
+    t_tensor = flops / (tflops_peak * 1e12)
+    t_hbm = nbytes / (hbm_peak * 1e9)
+    if flops > 0 and t_tensor >= t_hbm:
+        ach = flops / seconds / 1e12
+        return {"bound": "tensor", "achieved": round(ach, 1), "peak": tflops_peak, "unit": "TFLOP/s",
+                "frac": round(ach / tflops_peak, 4)}
+    ach = nbytes / seconds / 1e9
+    return {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s", "frac": round(ach / hbm_peak, 4)}
 
 
 def source_digest(name: str) -> str:
@@ -402,30 +417,25 @@ def run_ours(args, world, rank, local):
         entry = {"launches": n, "total_ms": round(ms, 4), "avg_us": round(1e3 * avg, 2),
                  "share": round(ms / sum(v[1] for v in prof_all.values()), 4)}
         if name in work:
-            unit, amount = work[name]
-            if unit == "flops":
-                entry["tflops"] = round(amount / (avg / 1e3) / 1e12, 1)
-                entry["frac_of_bf16_peak"] = round(amount / (avg / 1e3) / 1e12 / tflops, 3)
-            else:
-                entry["gbs"] = round(amount / (avg / 1e3) / 1e9, 1)
-                entry["frac_of_hbm"] = round(amount / (avg / 1e3) / 1e9 / hbm, 3)
+            fl, nb = work[name]
+            if fl:
+                entry["tflops"] = round(fl / (avg / 1e3) / 1e12, 1)
+                entry["frac_of_bf16_peak"] = round(fl / (avg / 1e3) / 1e12 / tflops, 3)
+            entry["gbs"] = round(nb / (avg / 1e3) / 1e9, 1)
+            entry["frac_of_hbm"] = round(nb / (avg / 1e3) / 1e9 / hbm, 3)
+            entry["bound"] = binding(fl, nb, avg / 1e3, tflops, hbm)["bound"]
         kernels[name] = entry
-    unit, amount = work.get(dom, ("flops", 0))
+    fl, nb = work.get(dom, (0, 0))
     avg_s = prof_dom[dom][1] / prof_dom[dom][0] / 1e3
-    if unit == "flops":
-        achieved = amount / avg_s / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": tflops, "unit": "TFLOP/s",
-                "frac": round(achieved / tflops, 4)}
-    else:
-        achieved = amount / avg_s / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4)}
+    roof = binding(fl, nb, avg_s, tflops, hbm)
+    roof["algorithmic_flops_per_launch"] = fl
+    roof["algorithmic_bytes_per_launch"] = nb
     roof["kernel"] = dom
     roof["launches_timed"] = prof_dom[dom][0]
     roof["traffic"] = committed_traffic(dom)
-    roof["peak_source"] = f"{peak_kind} ({'bf16_tflops_sustained' if unit == 'flops' else 'hbm_gbs'})"
+    roof["peak_source"] = f"{peak_kind} ({'bf16_tflops_sustained' if roof['bound'] == 'tensor' else 'hbm_gbs'})"
     gemm_names = [n for n in kernels if n.startswith("gemm_")]
-    gemm_flops = sum(work[n][1] * prof_all[n][0] for n in gemm_names)
+    gemm_flops = sum(work[n][0] * prof_all[n][0] for n in gemm_names)
     gemm_ms = sum(prof_all[n][1] for n in gemm_names)
     value = world * s.T * args.steps / (total_ms / 1e3)
     line = {

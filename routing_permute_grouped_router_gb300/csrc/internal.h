@@ -88,8 +88,9 @@ cudaError_t launch_combine_bwd(const Shape& s, const void* dy, const void* y_per
                                uint32_t* err, cudaStream_t st);
 cudaError_t launch_dx_router(const Shape& s, const void* dx_perm, const int32_t* row_of, const float* dl,
                              const float* W_r, float* W_rT, void* dx, uint32_t* err, cudaStream_t st);
-cudaError_t launch_dwr(const Shape& s, const void* x, const float* dl, float* dW_r, int accumulate,
+cudaError_t launch_dwr(const Shape& s, const void* x, const float* dl, float* partial, float* dW_r, int accumulate,
                        cudaStream_t st);
+int dwr_splits(const Shape& s);  // token slices of the router-weight gradient (partial buffer [splits][d][E])
 cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t st);
 
 // ---- gemm_tc.cu (bf16, tcgen05) and gemm_simt.cu (fp32) ----

@@ -187,7 +187,7 @@ struct FwdScratch {
 };
 struct BwdScratch {
   void *dy_perm, *da, *db, *dx_perm;
-  float *dg, *dl, *W_rT;
+  float *dg, *dl, *W_rT, *partial;
 };
 
 RoutingScratch carve_routing(Carver& c, const Shape& s) {
@@ -225,6 +225,7 @@ BwdScratch carve_bwd(Carver& c, const Shape& s) {
   b.dg = static_cast<float*>(c.take((size_t)s.T * s.k * 4));
   b.dl = static_cast<float*>(c.take((size_t)s.T * s.E * 4));
   b.W_rT = static_cast<float*>(c.take((size_t)s.E * s.d * 4));
+  b.partial = static_cast<float*>(c.take((size_t)dwr_splits(s) * s.d * s.E * 4));
   return b;
 }
 size_t ws_bytes_for(const Shape& s, int training) {
@@ -283,7 +284,7 @@ moe_status do_dx_router(const Shape& s, const void* x, const void* dx_perm, cons
     return MOE_OK;
   }
   CUDA_TRY(launch_dx_router(s, dx_perm, row_of, dl, W_r, bs.W_rT, dx, err, st));
-  CUDA_TRY(launch_dwr(s, x, dl, dW_r, accumulate, st));
+  CUDA_TRY(launch_dwr(s, x, dl, bs.partial, dW_r, accumulate, st));
   return MOE_OK;
 }
 

@@ -34,7 +34,8 @@ constexpr int R_MAXK = 8;
 
 template <int N>
 struct RCfg {
-  static constexpr int NST = N <= 64 ? 4 : 3;
+  // as many stages as fit in ~180 KB: small E leaves room for deep prefetch of x
+  static constexpr int NST = N <= 16 ? 8 : (N <= 32 ? 6 : (N <= 64 ? 4 : 3));
   static constexpr int A_BYTES = RT * RK * 2;
   static constexpr int B_BYTES = 3 * N * RK * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
@@ -83,8 +84,8 @@ __global__ void __launch_bounds__(R_THREADS, 1) router_tc_kernel(const __grid_co
   __shared__ int hist_s[2][R_MAXK][N];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::CTRL_OFF);
-  uint64_t* empty_bar = full_bar + 4;
-  uint64_t* tfull_bar = empty_bar + 4;
+  uint64_t* empty_bar = full_bar + 8;
+  uint64_t* tfull_bar = empty_bar + 8;
   uint64_t* drain_bar = tfull_bar + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);

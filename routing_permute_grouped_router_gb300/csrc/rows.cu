@@ -371,40 +371,44 @@ __global__ void __launch_bounds__(RW_WARPS * 32) dx_router_kernel(DxArgs a) {
 }
 
 // -------------------------------------------------------------------------- //
-// dW_r (+)= x^T dl in one pass.  A block owns 8 columns of x and 8 experts; its
-// 256 threads take the tokens round-robin, each accumulating an 8x8 fp32 tile,
-// then the block reduces the tiles in a fixed order (warp shuffles, then the
-// eight warps in index order): deterministic, no atomics, no second kernel.
+// dW_r (+)= x^T dl in two passes, deterministic and without atomics.  Pass 1:
+// a block owns 256 columns of x (8 per lane, so every warp load is one
+// contiguous 512-byte row segment), 8 experts and one slice of the tokens; its
+// warps take the slice's tokens round-robin, each lane accumulating an 8x8
+// fp32 tile, and the warps are summed in index order.  Pass 2 adds the slices
+// in slice order.
 // -------------------------------------------------------------------------- //
 constexpr int DW_THREADS = 256;
+constexpr int DW_COLS = 256;
 
 struct DwArgs {
   const void* x;
   const float* dl;
-  float* dW_r;
-  int T, d, E, accumulate;
+  float* partial;  // [splits][d][E]
+  int T, d, E, tok_per_split;
 };
 
 template <typename Tx>
-__global__ void __launch_bounds__(DW_THREADS) dwr_kernel(DwArgs a) {
-  __shared__ float part[DW_THREADS / 32][64];
+__global__ void __launch_bounds__(DW_THREADS) dwr_partial_kernel(DwArgs a) {
+  __shared__ float red[32][65];
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
-  const int e0 = blockIdx.x * 8, i0 = blockIdx.y * 8;  // experts fastest: neighbours share x columns
+  const int i0 = blockIdx.x * DW_COLS + lane * 8, s = blockIdx.y, e0 = blockIdx.z * 8;
+  const int tb = s * a.tok_per_split, te = min(a.T, tb + a.tok_per_split);
   const Tx* x = static_cast<const Tx*>(a.x);
-  const bool full_e = e0 + 8 <= a.E && (a.E % 4) == 0;
   const bool full_i = i0 + 8 <= a.d;
+  const bool full_e = e0 + 8 <= a.E && (a.E % 4) == 0;
   float acc[8][8];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
 #pragma unroll 4
-  for (int t = tid; t < a.T; t += DW_THREADS) {
+  for (int t = tb + warp; t < te; t += DW_THREADS / 32) {
     float xv[8], lv[8];
     if (full_i) {
       const Tx* xr = x + (size_t)t * a.d + i0;
       if (sizeof(Tx) == 2) {
-        unpack(*reinterpret_cast<const uint4*>(xr), xv);
+        unpack(ldg16(xr), xv);
       } else {
         const float4 p0 = reinterpret_cast<const float4*>(xr)[0], p1 = reinterpret_cast<const float4*>(xr)[1];
         xv[0] = p0.x; xv[1] = p0.y; xv[2] = p0.z; xv[3] = p0.w;
@@ -428,24 +432,31 @@ __global__ void __launch_bounds__(DW_THREADS) dwr_kernel(DwArgs a) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(xv[i], lv[e], acc[i][e]);
   }
+  // sum the 8 warps' tiles in warp order
+  for (int w = 0; w < DW_THREADS / 32; ++w) {
+    if (warp == w) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float v = warp_sum(acc[i][e]);
-      if (lane == 0) part[warp][i * 8 + e] = v;
+        for (int e = 0; e < 8; ++e) red[lane][i * 8 + e] = (w == 0 ? 0.f : red[lane][i * 8 + e]) + acc[i][e];
     }
-  __syncthreads();
-  if (tid < 64) {
-    const int i = i0 + tid / 8, e = e0 + tid % 8;
-    float s = 0.f;
-#pragma unroll
-    for (int w = 0; w < DW_THREADS / 32; ++w) s += part[w][tid];
-    if (i < a.d && e < a.E) {
-      float* o = a.dW_r + (size_t)i * a.E + e;
-      *o = a.accumulate ? *o + s : s;
-    }
+    __syncthreads();
   }
+  // write this slice's partial: 256 columns x 8 experts
+  for (int idx = tid; idx < DW_COLS * 8; idx += DW_THREADS) {
+    const int c = idx / 8, e = idx % 8;
+    const int i = blockIdx.x * DW_COLS + c;
+    if (i < a.d && e0 + e < a.E)
+      a.partial[((size_t)s * a.d + i) * a.E + e0 + e] = red[c / 8][(c % 8) * 8 + e];
+  }
+}
+
+__global__ void dwr_reduce_kernel(const float* partial, float* dW_r, int splits, int64_t n, int accumulate) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  float p = 0.f;
+  for (int q = 0; q < splits; ++q) p += partial[(size_t)q * n + i];
+  dW_r[i] = accumulate ? dW_r[i] + p : p;
 }
 
 int row_vecs(const Shape& s) { return s.d * (s.bf16 ? 2 : 4) / 16; }
@@ -544,13 +555,35 @@ cudaError_t launch_dx_router(const Shape& s, const void* dx_perm, const int32_t*
   return launch_typed_k<DxL>(s, a, (s.T + RW_WARPS - 1) / RW_WARPS, st);
 }
 
-cudaError_t launch_dwr(const Shape& s, const void* x, const float* dl, float* dW_r, int accumulate,
+int dwr_splits(const Shape& s) {
+  // about 32 tokens per warp (the loop is latency-bound), at least two blocks
+  // per SM, and at most 64 MB of partial sums
+  const int blocks = ((s.d + DW_COLS - 1) / DW_COLS) * ((s.E + 7) / 8);
+  int splits = (s.T + 255) / 256;
+  const int min_splits = (2 * 152 + blocks - 1) / blocks;
+  if (splits < min_splits) splits = min_splits;
+  const int64_t cap = ((int64_t)64 << 20) / ((int64_t)s.d * s.E * 4);
+  if (splits > cap) splits = (int)cap;
+  const int max_splits = (s.T + 63) / 64;
+  if (splits > max_splits) splits = max_splits;
+  return splits < 1 ? 1 : splits;
+}
+
+cudaError_t launch_dwr(const Shape& s, const void* x, const float* dl, float* partial, float* dW_r, int accumulate,
                        cudaStream_t st) {
-  DwArgs a{x, dl, dW_r, s.T, s.d, s.E, accumulate};
-  dim3 grid((s.E + 7) / 8, (s.d + 7) / 8);
-  LaunchScope ls(KK_DWR, st);
-  if (s.bf16) dwr_kernel<__nv_bfloat16><<<grid, DW_THREADS, 0, st>>>(a);
-  else dwr_kernel<float><<<grid, DW_THREADS, 0, st>>>(a);
+  const int splits = dwr_splits(s);
+  DwArgs a{x, dl, partial, s.T, s.d, s.E, (s.T + splits - 1) / splits};
+  {
+    dim3 grid((s.d + DW_COLS - 1) / DW_COLS, splits, (s.E + 7) / 8);
+    LaunchScope ls(KK_DWR, st);
+    if (s.bf16) dwr_partial_kernel<__nv_bfloat16><<<grid, DW_THREADS, 0, st>>>(a);
+    else dwr_partial_kernel<float><<<grid, DW_THREADS, 0, st>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t n = (int64_t)s.d * s.E;
+  LaunchScope ls(KK_DWR_REDUCE, st);
+  dwr_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(partial, dW_r, splits, n, accumulate);
   return cudaGetLastError();
 }
 
