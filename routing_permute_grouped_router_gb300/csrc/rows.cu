@@ -455,6 +455,7 @@ __global__ void dwr_reduce_kernel(const float* partial, float* dW_r, int splits,
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
   float p = 0.f;
+#pragma unroll 8
   for (int q = 0; q < splits; ++q) p += partial[(size_t)q * n + i];
   dW_r[i] = accumulate ? dW_r[i] + p : p;
 }
