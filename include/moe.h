@@ -272,6 +272,17 @@ moe_status moe_router_topk_noalloc(const moe_config* cfg, const void* x, const f
  * kernel and check; clear != 0 resets the word.  Either output may be NULL. */
 moe_status moe_get_device_error(int32_t* code, int32_t* detail, int clear);
 
+/* Self-test of failure detection (the pages have no counterpart; it checks
+ * this library's own safeguard).  Every mbarrier wait in the tensor-core
+ * kernels gives up after a time limit, records MOE_ERR_TIMEOUT in the device
+ * error word, drains and exits, so a stalled pipeline is reported rather than
+ * hanging the GPU.  This launches one thread that waits with that same helper
+ * on a barrier nothing arrives at (arrive = 0) or one that another warp
+ * arrives at (arrive = 1, the control), giving up after limit_ns nanoseconds
+ * (1e6 <= limit_ns <= 2e9).  Afterwards moe_get_device_error reports
+ * MOE_ERR_TIMEOUT (arrive = 0) or MOE_OK (arrive = 1); the GPU stays usable. */
+moe_status moe_selftest_bounded_wait(int64_t limit_ns, int arrive, moe_stream_t stream);
+
 /* Kernel launches the library has issued in this process (all devices). */
 uint64_t moe_launch_count(void);
 

@@ -75,6 +75,7 @@ _SIGNATURES = {
                       ctypes.POINTER(MoeGrads), _I, _P, _Z, _P],
     "moe_get_device_error": [ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32), _I],
     "moe_launch_count": [],
+    "moe_selftest_bounded_wait": [ctypes.c_int64, _I, _P],
     "moe_profiler_enable": [_I],
     "moe_kernel_kinds": [],
     "moe_profiler_filter": [ctypes.c_int32],
@@ -252,6 +253,12 @@ def moe_get_device_error(clear: bool = True):
     c, d = ctypes.c_int32(), ctypes.c_int32()
     _check("moe_get_device_error", lib().moe_get_device_error(ctypes.byref(c), ctypes.byref(d), int(clear)))
     return c.value, d.value
+
+
+def moe_selftest_bounded_wait(limit_ns: int, arrive: bool, stream=None) -> None:
+    """Run the bounded-wait self-test kernel (see include/moe.h)."""
+    _check("moe_selftest_bounded_wait",
+           lib().moe_selftest_bounded_wait(int(limit_ns), int(arrive), _stream(stream)))
 
 
 def moe_launch_count() -> int:

@@ -26,6 +26,7 @@ enum KernelKind : int {
   KK_DWR_REDUCE,
   KK_ZERO,
   KK_SPLIT_WR,
+  KK_SELFTEST,
   KK_COUNT
 };
 

@@ -77,7 +77,7 @@ cudaEvent_t pool_event() {
 const char* const kKernelNames[KK_COUNT] = {
     "router_topk",  "slot_scan",  "slot_assign",     "permute",      "gemm_up_swiglu", "gemm_down",
     "unpermute_combine", "combine_bwd", "gemm_dgrad_h_swiglu_bwd", "gemm_wgrad", "gemm_dgrad_x",
-    "transpose_wr", "dx_router",  "dwr",     "dwr_reduce",   "zero", "split_wr"};
+    "transpose_wr", "dx_router",  "dwr",     "dwr_reduce",   "zero", "split_wr", "selftest_bounded_wait"};
 
 }  // namespace
 

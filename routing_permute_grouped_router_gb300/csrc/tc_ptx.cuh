@@ -46,14 +46,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Wait for the phase of `parity` to complete.  Gives up after WAIT_LIMIT_NS or
 // when another role has raised the abort flag; returns false then.
 __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t* err,
-                                       uint32_t where) {
+                                       uint32_t where, uint64_t limit_ns = WAIT_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1; i < (1u << 30); ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 255u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > WAIT_LIMIT_NS) break;
+      if (globaltimer() - t0 > limit_ns) break;
     }
   }
   *abort_flag = 1;

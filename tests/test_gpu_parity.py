@@ -262,3 +262,24 @@ def test_corrupt_routing_state_is_reported_not_followed():
                         L.weights["W2"], L.saved["h"], L.saved["y_perm"])
     code, _ = pkg.moe_get_device_error(clear=True)
     assert pkg.STATUS[code] == "MOE_ERR_DEVICE_CHECK"
+
+
+# ------------------------------ failure detection ------------------------- #
+def test_bounded_wait_reports_timeout_and_gpu_stays_usable():
+    """A pipeline wait that nothing satisfies gives up after its limit and
+    reports MOE_ERR_TIMEOUT; the control (a warp arrives) reports nothing, and
+    a full layer step runs correctly afterwards."""
+    import time
+
+    pkg.moe_get_device_error(clear=True)
+    pkg.moe_selftest_bounded_wait(50_000_000, arrive=True)
+    code, _ = pkg.moe_get_device_error(clear=True)
+    assert code == 0
+    t0 = time.perf_counter()
+    pkg.moe_selftest_bounded_wait(50_000_000, arrive=False)
+    code, detail = pkg.moe_get_device_error(clear=True)
+    waited = time.perf_counter() - t0
+    assert pkg.STATUS[code] == "MOE_ERR_TIMEOUT"
+    assert (detail & 0xFFFFFF) == 700
+    assert 0.04 < waited < 5.0
+    test_layer_forward("top2_e8_small")
