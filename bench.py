@@ -182,8 +182,9 @@ def source_digest(name: str) -> str:
     return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
 
 
-def committed_traffic(name: str):
-    """DRAM bytes per launch from the committed ncu summary, if it matches the current source."""
+def committed_traffic(name: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this
+    workload and matches the current source."""
     if not os.path.exists(PROFILE_FILE):
         return None
     vals = {}
@@ -193,7 +194,7 @@ def committed_traffic(name: str):
             vals[key.strip()] = v.strip()
     tb = vals.get(f"traffic.{name}.bytes_per_launch")
     sha = vals.get(f"traffic.{name}.source_sha")
-    if tb is None or sha != source_digest(name):
+    if tb is None or sha != source_digest(name) or vals.get("traffic.workload") != workload:
         return None
     return float(tb)
 
@@ -432,7 +433,7 @@ def run_ours(args, world, rank, local):
     roof["algorithmic_bytes_per_launch"] = nb
     roof["kernel"] = dom
     roof["launches_timed"] = prof_dom[dom][0]
-    roof["traffic"] = committed_traffic(dom)
+    roof["traffic"] = committed_traffic(dom, args.workload)
     roof["peak_source"] = f"{peak_kind} ({'bf16_tflops_sustained' if roof['bound'] == 'tensor' else 'hbm_gbs'})"
     gemm_names = [n for n in kernels if n.startswith("gemm_")]
     gemm_flops = sum(work[n][0] * prof_all[n][0] for n in gemm_names)

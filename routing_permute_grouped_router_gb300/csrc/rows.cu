@@ -371,83 +371,86 @@ __global__ void __launch_bounds__(RW_WARPS * 32) dx_router_kernel(DxArgs a) {
 }
 
 // -------------------------------------------------------------------------- //
-// dW_r (+)= x^T dl in two passes, deterministic and without atomics.  Pass 1:
-// a block owns 256 columns of x (8 per lane, so every warp load is one
-// contiguous 512-byte row segment), 8 experts and one slice of the tokens; its
-// warps take the slice's tokens round-robin, each lane accumulating an 8x8
-// fp32 tile, and the warps are summed in index order.  Pass 2 adds the slices
-// in slice order.
+// dW_r (+)= x^T dl in two passes, deterministic and without atomics.  dl has at
+// most k nonzero experts per token when k > 1, so the product is taken
+// sparsely.  Pass 1: a block owns 64 columns of x and one slice of the tokens;
+// each warp takes a sub-slice in token order, lane l owning columns 2l, 2l+1,
+// and adds dl[t,e] * x[t, cols] into its private shared-memory accumulator row
+// e for every e with dl[t,e] != 0 (found with a ballot).  The block then sums
+// its warps in index order and writes the slice's partial.  Pass 2 adds the
+// slices in slice order.
 // -------------------------------------------------------------------------- //
-constexpr int DW_THREADS = 256;
-constexpr int DW_COLS = 256;
+constexpr int DW_COLS = 64;
+constexpr int DW_STRIDE = DW_COLS + 2;  // accumulator row pitch: float2 adds stay aligned, column reads spread over banks
+constexpr int DW_BATCH = 8;             // tokens whose loads a warp issues together
 
 struct DwArgs {
   const void* x;
   const float* dl;
   float* partial;  // [splits][d][E]
-  int T, d, E, tok_per_split;
+  int T, d, E, tok_per_split, warps;
 };
 
+__device__ __forceinline__ float2 load_pair(const float* p) { return *reinterpret_cast<const float2*>(p); }
+__device__ __forceinline__ float2 load_pair(const __nv_bfloat16* p) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+
 template <typename Tx>
-__global__ void __launch_bounds__(DW_THREADS) dwr_partial_kernel(DwArgs a) {
-  __shared__ float red[32][65];
+__global__ void __launch_bounds__(256) dwr_partial_kernel(DwArgs a) {
+  extern __shared__ float dw_acc[];  // [warps][E][DW_STRIDE]
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
-  const int i0 = blockIdx.x * DW_COLS + lane * 8, s = blockIdx.y, e0 = blockIdx.z * 8;
-  const int tb = s * a.tok_per_split, te = min(a.T, tb + a.tok_per_split);
+  const int i0 = blockIdx.x * DW_COLS, s = blockIdx.y;
+  const int col = i0 + 2 * lane;
+  const bool has_col = col < a.d;  // d is even for both dtypes
+  const int chunks = (a.E + 31) / 32;
+  float* acc = dw_acc + (size_t)warp * a.E * DW_STRIDE;
+  for (int i = lane; i < a.E * DW_STRIDE; i += 32) acc[i] = 0.f;
+  __syncwarp();
+  const int sb = s * a.tok_per_split, se = min(a.T, sb + a.tok_per_split);
+  const int per = (se - sb + a.warps - 1) / a.warps;
+  const int tb = sb + warp * per, te = min(se, tb + per);
   const Tx* x = static_cast<const Tx*>(a.x);
-  const bool full_i = i0 + 8 <= a.d;
-  const bool full_e = e0 + 8 <= a.E && (a.E % 4) == 0;
-  float acc[8][8];
+  for (int t0 = tb; t0 < te; t0 += DW_BATCH) {
+    float2 xv[DW_BATCH];
+    float lv[DW_BATCH][4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+    for (int b = 0; b < DW_BATCH; ++b) {
+      const int t = t0 + b;
+      const bool ok = t < te;
+      xv[b] = (ok && has_col) ? load_pair(x + (size_t)t * a.d + col) : make_float2(0.f, 0.f);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
-#pragma unroll 4
-  for (int t = tb + warp; t < te; t += DW_THREADS / 32) {
-    float xv[8], lv[8];
-    if (full_i) {
-      const Tx* xr = x + (size_t)t * a.d + i0;
-      if (sizeof(Tx) == 2) {
-        unpack(ldg16(xr), xv);
-      } else {
-        const float4 p0 = reinterpret_cast<const float4*>(xr)[0], p1 = reinterpret_cast<const float4*>(xr)[1];
-        xv[0] = p0.x; xv[1] = p0.y; xv[2] = p0.z; xv[3] = p0.w;
-        xv[4] = p1.x; xv[5] = p1.y; xv[6] = p1.z; xv[7] = p1.w;
+      for (int c = 0; c < 4; ++c) {
+        const int e = 32 * c + lane;
+        lv[b][c] = (ok && c < chunks && e < a.E) ? a.dl[(size_t)t * a.E + e] : 0.f;
       }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) xv[i] = (i0 + i < a.d) ? to_f32(x[(size_t)t * a.d + i0 + i]) : 0.f;
-    }
-    const float* lr = a.dl + (size_t)t * a.E + e0;
-    if (full_e) {
-      const float4 q0 = reinterpret_cast<const float4*>(lr)[0], q1 = reinterpret_cast<const float4*>(lr)[1];
-      lv[0] = q0.x; lv[1] = q0.y; lv[2] = q0.z; lv[3] = q0.w;
-      lv[4] = q1.x; lv[5] = q1.y; lv[6] = q1.z; lv[7] = q1.w;
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) lv[e] = (e0 + e < a.E) ? lr[e] : 0.f;
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int b = 0; b < DW_BATCH; ++b) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(xv[i], lv[e], acc[i][e]);
+      for (int c = 0; c < 4; ++c) {
+        if (c >= chunks) break;  // warp-uniform
+        unsigned nz = __ballot_sync(0xffffffffu, lv[b][c] != 0.f);
+        while (nz) {  // the experts of this token with a nonzero logit gradient, in expert order
+          const int src = __ffs(nz) - 1;
+          nz &= nz - 1;
+          const float w = __shfl_sync(0xffffffffu, lv[b][c], src);
+          float2* r = reinterpret_cast<float2*>(acc + (size_t)(32 * c + src) * DW_STRIDE + 2 * lane);
+          float2 v = *r;
+          v.x = fmaf(w, xv[b].x, v.x);
+          v.y = fmaf(w, xv[b].y, v.y);
+          *r = v;
+        }
+      }
+    }
   }
-  // sum the 8 warps' tiles in warp order
-  for (int w = 0; w < DW_THREADS / 32; ++w) {
-    if (warp == w) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) red[lane][i * 8 + e] = (w == 0 ? 0.f : red[lane][i * 8 + e]) + acc[i][e];
-    }
-    __syncthreads();
-  }
-  // write this slice's partial: 256 columns x 8 experts
-  for (int idx = tid; idx < DW_COLS * 8; idx += DW_THREADS) {
-    const int c = idx / 8, e = idx % 8;
-    const int i = blockIdx.x * DW_COLS + c;
-    if (i < a.d && e0 + e < a.E)
-      a.partial[((size_t)s * a.d + i) * a.E + e0 + e] = red[c / 8][(c % 8) * 8 + e];
+  __syncthreads();
+  // sum the warps in index order; write this slice's partial [d][E]
+  for (int idx = tid; idx < a.E * DW_COLS; idx += blockDim.x) {
+    const int c = idx / a.E, e = idx % a.E;  // consecutive threads: consecutive experts of one column
+    float v = 0.f;
+    for (int w = 0; w < a.warps; ++w) v += dw_acc[((size_t)w * a.E + e) * DW_STRIDE + c];
+    if (i0 + c < a.d) a.partial[((size_t)s * a.d + i0 + c) * a.E + e] = v;
   }
 }
 
@@ -556,29 +559,43 @@ cudaError_t launch_dx_router(const Shape& s, const void* dx_perm, const int32_t*
   return launch_typed_k<DxL>(s, a, (s.T + RW_WARPS - 1) / RW_WARPS, st);
 }
 
+// Warps per block: the private accumulators stay near 66 KB so that three
+// blocks fit on an SM.
+int dwr_warps(const Shape& s) { return s.E <= 32 ? 8 : (s.E <= 64 ? 4 : 2); }
+
 int dwr_splits(const Shape& s) {
-  // about 32 tokens per warp (the loop is latency-bound), at least two blocks
-  // per SM, and at most 64 MB of partial sums
-  const int blocks = ((s.d + DW_COLS - 1) / DW_COLS) * ((s.E + 7) / 8);
-  int splits = (s.T + 255) / 256;
-  const int min_splits = (2 * 152 + blocks - 1) / blocks;
-  if (splits < min_splits) splits = min_splits;
-  const int64_t cap = ((int64_t)64 << 20) / ((int64_t)s.d * s.E * 4);
-  if (splits > cap) splits = (int)cap;
-  const int max_splits = (s.T + 63) / 64;
-  if (splits > max_splits) splits = max_splits;
+  const int warps = dwr_warps(s), col_blocks = (s.d + DW_COLS - 1) / DW_COLS;
+  int splits = (s.T + 64 * warps - 1) / (64 * warps);  // 64 tokens a warp
+  const int want = (4 * 152 + col_blocks - 1) / col_blocks;  // about four blocks an SM
+  if (splits < want) splits = std::min(want, (s.T + 16 * warps - 1) / (16 * warps));  // at least 16 tokens a warp
+  const int64_t cap = ((int64_t)64 << 20) / ((int64_t)s.d * s.E * 4);  // partials within 64 MB
+  if (splits > cap) splits = (int)std::max<int64_t>(cap, 1);
+  if (splits > 65535) splits = 65535;  // grid y limit
   return splits < 1 ? 1 : splits;
 }
 
 cudaError_t launch_dwr(const Shape& s, const void* x, const float* dl, float* partial, float* dW_r, int accumulate,
                        cudaStream_t st) {
-  const int splits = dwr_splits(s);
-  DwArgs a{x, dl, partial, s.T, s.d, s.E, (s.T + splits - 1) / splits};
+  const int splits = dwr_splits(s), warps = dwr_warps(s);
+  DwArgs a{x, dl, partial, s.T, s.d, s.E, (s.T + splits - 1) / splits, warps};
+  const size_t smem = (size_t)warps * s.E * DW_STRIDE * 4;
   {
-    dim3 grid((s.d + DW_COLS - 1) / DW_COLS, splits, (s.E + 7) / 8);
+    static bool attr_done[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (!attr_done[dev]) {
+      cudaError_t e1 = cudaFuncSetAttribute(dwr_partial_kernel<__nv_bfloat16>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+      cudaError_t e2 = cudaFuncSetAttribute(dwr_partial_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            96 * 1024);
+      if (e1 != cudaSuccess || e2 != cudaSuccess) return e1 != cudaSuccess ? e1 : e2;
+      attr_done[dev] = true;
+    }
+    dim3 grid((s.d + DW_COLS - 1) / DW_COLS, splits);
     LaunchScope ls(KK_DWR, st);
-    if (s.bf16) dwr_partial_kernel<__nv_bfloat16><<<grid, DW_THREADS, 0, st>>>(a);
-    else dwr_partial_kernel<float><<<grid, DW_THREADS, 0, st>>>(a);
+    if (s.bf16) dwr_partial_kernel<__nv_bfloat16><<<grid, warps * 32, smem, st>>>(a);
+    else dwr_partial_kernel<float><<<grid, warps * 32, smem, st>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
