@@ -436,7 +436,7 @@ def run_ours(args, world, rank, local):
     roof["traffic"] = committed_traffic(dom, args.workload)
     roof["peak_source"] = f"{peak_kind} ({'bf16_tflops_sustained' if roof['bound'] == 'tensor' else 'hbm_gbs'})"
     gemm_names = [n for n in kernels if n.startswith("gemm_")]
-    gemm_flops = sum(work[n][0] * prof_all[n][0] for n in gemm_names)
+    gemm_flops = sum(work.get(n, (0, 0))[0] * prof_all[n][0] for n in gemm_names)  # the tail fixup adds time, no FLOPs
     gemm_ms = sum(prof_all[n][1] for n in gemm_names)
     value = world * s.T * args.steps / (total_ms / 1e3)
     line = {

@@ -11,19 +11,27 @@
 //   DGRAD_X dx_perm = [da | db] [W1_e | W3_e]^T (K concatenated)          A K-major, B K-major
 //   WGRAD   dW1_e = X_e^T da, dW3_e = X_e^T db, dW2_e = H_e^T dY_e (fp32)  A MN-major, B MN-major
 //
-// Structure (one CTA per SM, 192 threads):
-//   warp 0, one lane: TMA producer; 128x64 A and 256x64 B bf16 tiles in
-//     128-byte-swizzled shared memory, 4-stage mbarrier ring;
-//   warp 1: allocates 512 TMEM columns; one lane issues tcgen05.mma
-//     (M=128, N=256, K=16, fp32 accumulate) into one of two 256-column
-//     accumulators and commits stage releases and accumulator-ready events;
-//   warps 2-5: epilogue; tcgen05.ld moves a 32-row x 32-column slice per
-//     warp into registers, the fused math runs there, results go to HBM.
-// Tiles are taken round-robin from a list the kernel derives on the device
-// from offsets/counts, so the host never reads the routing outcome.  Every
-// mbarrier wait is bounded (2 s); on expiry the kernel records
-// DEV_TIMEOUT in the error word, drains its own copies and MMAs, frees TMEM
-// and exits.
+// Structure: CTA pairs (clusters of two, one CTA per SM, 192 threads each).
+// A pair computes a 256 x 256 tile with the 2-SM tcgen05 MMA: each CTA stages
+// its own 128 rows of A and one half (128 columns) of B, and its TMEM receives
+// its 128 rows of the fp32 accumulator.  Per 256 x 256 x 64 step an SM thus
+// reads 32 KB of operands instead of the 48 KB a single-SM 128 x 256 tile
+// needs for half the work, and six stages fit in shared memory.
+//   warp 0, one lane: TMA producer of this CTA's halves, 6-stage ring (5 for
+//     dgrad h); the byte count of both CTAs lands on the first CTA's barrier;
+//   warp 1: allocates TMEM with its peer; in the first CTA one lane issues
+//     tcgen05.mma.cta_group::2 (M=256, N=256, K=16) and commits stage
+//     releases and accumulator-ready events to the barriers of both CTAs;
+//   warps 2-5 of both CTAs: epilogue of their own rows; tcgen05.ld moves a
+//     32-row x 32-column slice per warp into registers, the fused math runs
+//     there, results go to HBM by TMA; they release the accumulator on the
+//     first CTA's barrier.
+// Tiles are taken round-robin over the pairs from a list the kernel derives on
+// the device from offsets/counts, so the host never reads the routing outcome.
+// Expert segments are 128-row aligned, so the second half of an expert's last
+// pair tile may lie outside the expert: it is computed and not stored.  Every
+// mbarrier wait is bounded (2 s); on expiry the kernel records DEV_TIMEOUT in
+// the error word, drains its own copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -33,33 +41,45 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int A_BYTES = BM * BK * 2;  // 16 KB
-constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int BM = 128, BN = 256, BK = 64;  // BM: rows per CTA (the pair covers 2 * BM)
+constexpr int BNH = BN / 2;                 // B columns staged by each CTA of the pair
+constexpr int A_BYTES = BM * BK * 2;        // 16 KB
+constexpr int B_BYTES = BNH * BK * 2;       // 16 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int PAIR_STAGE_BYTES = 2 * STAGE_BYTES;  // bytes both CTAs land on the first CTA's full barrier
 constexpr int CTRL_BYTES = 2048;
 constexpr int THREADS = 192;
 constexpr int EPI_WARPS = 4;
 constexpr int BOX_BYTES = 4096;  // one staged output box: 32 rows x 128 bytes
-constexpr uint32_t TMEM_COLS = 512;
+constexpr int ACC_BUFS = 2;      // TMEM accumulators (256 columns each)
+constexpr uint32_t TMEM_COLS = 256 * ACC_BUFS;
 constexpr int MAX_E = 128;
 constexpr int MAX_SMEM = 232448;  // 227 KB per CTA
+constexpr int MAX_ST = 6;
+constexpr int WG_AHEAD = 2;  // wgrad: old-gradient boxes requested ahead of the one being added
 
 enum Mode { M_UP = 0, M_DOWN = 1, M_DGRAD_H = 2, M_DGRAD_X = 3, M_WGRAD = 4 };
 
 // Pipeline depth and epilogue staging per product.  Each epilogue warp owns two
-// output boxes (double buffering of its TMA stores); dgrad h also stages its a
-// and b inputs, so it gives up one mainloop stage for four boxes per warp.
+// output boxes (double buffering of its TMA stores).  dgrad h also stages its a
+// and b inputs, and wgrad the old fp32 gradient it adds to; both give up one
+// mainloop stage for four boxes per warp.
+static_assert(MAX_ST >= 6, "barrier arrays");
+// control block: 33 mbarriers and 4 words below byte 320, then offsets, counts and pair prefixes
+static_assert((2 * MAX_ST + 5 + 4 * 4) * 8 + 16 <= 320, "control block");
+static_assert(320 + (3 * 128 + 2) * 4 <= 2048, "control block");
 template <int MODE>
 struct ModeCfg {
-  static constexpr int NST = MODE == M_DGRAD_H ? 3 : 4;
-  static constexpr int EPI_WARP_BYTES = (MODE == M_DGRAD_H ? 4 : 2) * BOX_BYTES;
+  static constexpr bool WIDE = MODE == M_DGRAD_H || MODE == M_WGRAD;  // four staged boxes per warp
+  static constexpr int NST = WIDE ? 5 : 6;
+  static constexpr int EPI_WARP_BYTES = (WIDE ? 4 : 2) * BOX_BYTES;
   static constexpr int EPI_OFF = NST * STAGE_BYTES;
   static constexpr int CTRL_OFF = EPI_OFF + EPI_WARPS * EPI_WARP_BYTES;
   static constexpr int SMEM = CTRL_OFF + CTRL_BYTES + 1024;  // + alignment slack
 };
 static_assert(ModeCfg<M_UP>::SMEM <= MAX_SMEM, "shared memory budget");
 static_assert(ModeCfg<M_DGRAD_H>::SMEM <= MAX_SMEM, "shared memory budget");
+static_assert(ModeCfg<M_WGRAD>::SMEM <= MAX_SMEM, "shared memory budget");
 
 // Tensor maps per product (loads of the mainloop first, then epilogue maps):
 //   UP      0 x_perm, 1 W1, 2 W3, 3 h (store), 4 a (store), 5 b (store)
@@ -88,10 +108,11 @@ struct TcArgs {
   uint32_t* err;
 };
 
-// Instruction descriptor of kind::f16: fp32 D, bf16 A and B, M = 128, N = 256.
+// Instruction descriptor of kind::f16: fp32 D, bf16 A and B, M = 256 (the
+// pair), N = 256.
 __host__ __device__ constexpr uint32_t idesc_bf16(bool a_mn, bool b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
-         ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+         ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((2 * BM) >> 4) << 24);
 }
 
 // silu and sigmoid with the fast intrinsic divide (about 2 ulp; the results
@@ -146,12 +167,14 @@ __device__ __forceinline__ void regs_to_f32(const uint32_t (&r)[32], float (&v)[
 }
 
 // ------------------------------ tile schedule ------------------------------ //
+// A pair tile is 256 rows (this CTA: the half `rank`) by 256 columns.
 struct Tile {
   int e;
-  int64_t row0;  // first row of the tile (ragged-M modes) / first K row (WGRAD)
-  int m0, n0;    // WGRAD: output tile origin; other modes: n0 only
+  int64_t row0;  // ragged-M modes: this CTA's first row; WGRAD: first K row
+  int m0, n0;    // WGRAD: this CTA's output rows m0.. and the tile's columns n0..; others: n0
   int sub;       // WGRAD product: 0 = dW1, 1 = dW3, 2 = dW2
   int kblocks;
+  bool valid;    // this CTA's rows belong to the tile's expert
 };
 
 template <int MODE>
@@ -161,80 +184,98 @@ __device__ __forceinline__ int n_tiles_of(const TcArgs& a) {
   return a.f / BN;  // DGRAD_H
 }
 
+// s_pair[e]: pair tiles (of 2 x 128 rows) before expert e in the ragged-M modes.
 template <int MODE>
-__device__ __forceinline__ Tile decode(int tile, const TcArgs& a, const int* s_off, const int* s_cnt) {
+__device__ __forceinline__ Tile decode(int tile, uint32_t rank, const TcArgs& a, const int* s_off, const int* s_cnt,
+                                       const int* s_pair) {
   Tile t{};
+  t.valid = true;
   if (MODE == M_WGRAD) {
-    const int P = (a.d / BM) * (a.f / BN);
+    const int P = (a.d / (2 * BM)) * (a.f / BN);  // pair tiles of one product of one expert
     t.e = tile / (3 * P);
     const int q = tile % (3 * P);
+    int r, nt;
     if (q < 2 * P) {
       t.sub = q & 1;
-      const int r = q >> 1, nt = a.f / BN;
-      t.m0 = (r / nt) * BM;
-      t.n0 = (r % nt) * BN;
+      r = q >> 1;
+      nt = a.f / BN;
     } else {
       t.sub = 2;
-      const int r = q - 2 * P, nt = a.d / BN;
-      t.m0 = (r / nt) * BM;
-      t.n0 = (r % nt) * BN;
+      r = q - 2 * P;
+      nt = a.d / BN;
     }
+    t.m0 = (r / nt) * 2 * BM + (int)rank * BM;
+    t.n0 = (r % nt) * BN;
     t.row0 = s_off[t.e];
     t.kblocks = (s_cnt[t.e] + BK - 1) / BK;
   } else {
+    // expert e owns tiles [s_pair[e] * nt, s_pair[e + 1] * nt); inside it the
+    // row pairs run fastest, so the CTAs working at one time share a few weight
+    // column blocks and the expert's weights stream in over its whole run
     const int nt = n_tiles_of<MODE>(a);
-    const int mt = tile / nt;
-    t.n0 = (tile % nt) * (MODE == M_UP ? 128 : BN);
-    t.row0 = (int64_t)mt * BM;
+    const int q = tile / nt;
     int lo = 0, hi = a.E - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (s_off[mid] <= t.row0) lo = mid;
+      if (s_pair[mid] <= q) lo = mid;
       else hi = mid - 1;
     }
     t.e = lo;
+    const int pe = s_pair[t.e + 1] - s_pair[t.e];  // >= 1: q falls in this expert
+    const int l = tile - s_pair[t.e] * nt;
+    t.n0 = (l / pe) * (MODE == M_UP ? 128 : BN);
+    const int local = 2 * (l % pe) + (int)rank;
+    t.valid = local < (s_off[t.e + 1] - s_off[t.e]) / BM;
+    t.row0 = (int64_t)s_off[t.e] + (int64_t)local * BM;
     const int K = (MODE == M_UP || MODE == M_DGRAD_H) ? a.d : (MODE == M_DOWN ? a.f : 2 * a.f);
     t.kblocks = K / BK;
   }
   return t;
 }
 
+// This CTA's half of one stage: its 128 rows of A and its 128 columns of B.
+// bar is the first CTA's full barrier (a shared::cluster address in the second).
 template <int MODE>
 __device__ __forceinline__ void issue_stage(const TcMaps& maps, const TcArgs& a, const Tile& t, int kb, uint32_t sA,
-                                            uint32_t sB, uint32_t bar) {
+                                            uint32_t sB, uint32_t bar, uint32_t rank) {
+  auto ld = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1) {
+    if (rank == 0) tma_load_2d(dst, m, bar, c0, c1);
+    else tma_load_2d_pair(dst, m, bar, c0, c1);
+  };
   const int r0 = static_cast<int>(t.row0);
+  const int nh = (int)rank * BNH;  // this CTA's B columns start here
   if (MODE == M_UP) {
-    tma_load_2d(sA, &maps.m[0], bar, kb * BK, r0);
+    // B = [W1 columns n0.. | W3 columns n0..]: the first CTA stages the W1 half
+    ld(sA, &maps.m[0], kb * BK, r0);
+    const CUtensorMap* bm = rank == 0 ? &maps.m[1] : &maps.m[2];
     const int wr = t.e * a.d + kb * BK;
-    tma_load_2d(sB + 0 * 8192, &maps.m[1], bar, t.n0, wr);
-    tma_load_2d(sB + 1 * 8192, &maps.m[1], bar, t.n0 + 64, wr);
-    tma_load_2d(sB + 2 * 8192, &maps.m[2], bar, t.n0, wr);
-    tma_load_2d(sB + 3 * 8192, &maps.m[2], bar, t.n0 + 64, wr);
+    ld(sB, bm, t.n0, wr);
+    ld(sB + 8192, bm, t.n0 + 64, wr);
   } else if (MODE == M_DOWN) {
-    tma_load_2d(sA, &maps.m[0], bar, kb * BK, r0);
+    ld(sA, &maps.m[0], kb * BK, r0);
     const int wr = t.e * a.f + kb * BK;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) tma_load_2d(sB + c * 8192, &maps.m[1], bar, t.n0 + 64 * c, wr);
+    ld(sB, &maps.m[1], t.n0 + nh, wr);
+    ld(sB + 8192, &maps.m[1], t.n0 + nh + 64, wr);
   } else if (MODE == M_DGRAD_H) {
-    tma_load_2d(sA, &maps.m[0], bar, kb * BK, r0);
-    tma_load_2d(sB, &maps.m[1], bar, kb * BK, t.e * a.f + t.n0);
+    ld(sA, &maps.m[0], kb * BK, r0);
+    ld(sB, &maps.m[1], kb * BK, t.e * a.f + t.n0 + nh);
   } else if (MODE == M_DGRAD_X) {
     const int kf = a.f / BK;
     if (kb < kf) {
-      tma_load_2d(sA, &maps.m[0], bar, kb * BK, r0);
-      tma_load_2d(sB, &maps.m[2], bar, kb * BK, t.e * a.d + t.n0);
+      ld(sA, &maps.m[0], kb * BK, r0);
+      ld(sB, &maps.m[2], kb * BK, t.e * a.d + t.n0 + nh);
     } else {
-      tma_load_2d(sA, &maps.m[1], bar, (kb - kf) * BK, r0);
-      tma_load_2d(sB, &maps.m[3], bar, (kb - kf) * BK, t.e * a.d + t.n0);
+      ld(sA, &maps.m[1], (kb - kf) * BK, r0);
+      ld(sB, &maps.m[3], (kb - kf) * BK, t.e * a.d + t.n0 + nh);
     }
   } else {  // WGRAD
     const CUtensorMap* am = t.sub == 2 ? &maps.m[1] : &maps.m[0];
     const CUtensorMap* bm = t.sub == 0 ? &maps.m[2] : (t.sub == 1 ? &maps.m[3] : &maps.m[4]);
     const int kr = r0 + kb * BK;
-    tma_load_2d(sA, am, bar, t.m0, kr);
-    tma_load_2d(sA + 8192, am, bar, t.m0 + 64, kr);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) tma_load_2d(sB + c * 8192, bm, bar, t.n0 + 64 * c, kr);
+    ld(sA, am, t.m0, kr);
+    ld(sA + 8192, am, t.m0 + 64, kr);
+    ld(sB, bm, t.n0 + nh, kr);
+    ld(sB + 8192, bm, t.n0 + nh + 64, kr);
   }
 }
 
@@ -247,8 +288,8 @@ __device__ __forceinline__ void issue_stage(const TcMaps& maps, const TcArgs& a,
 // previous one drains.
 struct EpiState {
   uint32_t nbox;     // boxes this warp has staged so far (selects the buffer)
-  uint32_t uses[2];  // completed waits on the two input barriers (dgrad h)
-  bool pending[2];   // an input load is in flight into buffer h (dgrad h)
+  uint32_t uses[4];  // completed waits on the input barriers of the four buffers
+  bool pending[4];   // an input load is in flight into buffer h
 };
 
 // Stage and store one bf16 output box of 64 columns taken from 2 TMEM slices.
@@ -269,6 +310,11 @@ template <int MODE>
 __device__ __forceinline__ bool epilogue_tile(const TcMaps& maps, const TcArgs& a, const Tile& t, uint32_t tacc,
                                               int q, int lane, uint32_t ebuf, uint32_t lbar, EpiState& es,
                                               uint32_t tfull, uint32_t tfull_parity, volatile int* abort_flag) {
+  if (!t.valid) {  // rows outside the expert: nothing to store
+    if (!mbar_wait(tfull, tfull_parity, abort_flag, a.err, 400 + MODE)) return false;
+    tc_fence_after();
+    return true;
+  }
   const int row0 = static_cast<int>(t.row0) + q * 32;
   if (MODE == M_DGRAD_H) {
     // fetch the first a/b boxes of the tile while its mainloop still runs
@@ -290,14 +336,19 @@ __device__ __forceinline__ bool epilogue_tile(const TcMaps& maps, const TcArgs& 
   const CUtensorMap* wg_map = &maps.m[MODE == M_WGRAD ? 5 + t.sub : 0];
   const int wg_orow = t.e * wg_rows + t.m0 + q * 32;
   if (wg_add) {
-    const uint32_t h = es.nbox & 1;
-    if (lane == 0) {
-      bulk_wait_read0();
-      const uint32_t bar = lbar + 8 * h;
-      mbar_expect_tx(bar, BOX_BYTES);
-      tma_load_2d(ebuf + h * BOX_BYTES, wg_map, bar, t.n0, wg_orow);
+    // boxes 0 and 1 of the tile: their buffers were last read by the stores of
+    // boxes nbox-4 and nbox-3, older than the two latest stores
+    if (lane == 0) bulk_wait_read2();
+#pragma unroll
+    for (int c = 0; c < WG_AHEAD; ++c) {
+      const uint32_t h = (es.nbox + c) & 3u;
+      if (lane == 0) {
+        const uint32_t bar = lbar + 8 * h;
+        mbar_expect_tx(bar, BOX_BYTES);
+        tma_load_2d(ebuf + h * BOX_BYTES, wg_map, bar, t.n0 + c * 32, wg_orow);
+      }
+      es.pending[h] = true;
     }
-    es.pending[h] = true;
     __syncwarp();
   }
   if (!mbar_wait(tfull, tfull_parity, abort_flag, a.err, 400 + MODE)) return false;
@@ -410,17 +461,19 @@ __device__ __forceinline__ bool epilogue_tile(const TcMaps& maps, const TcArgs& 
     }
     es.nbox += 4;
   } else if (wg_add) {  // WGRAD, accumulate: dW += acc via TMA load, add, TMA store
+    // four buffers per warp; the old values of box c + 2 are requested while
+    // box c is added, so two loads are in flight behind the one being used
 #pragma unroll 1
     for (int c = 0; c < 8; ++c) {
-      const uint32_t h = (es.nbox + c) & 1;
-      const uint32_t buf = ebuf + h * BOX_BYTES;
-      if (c + 1 < 8) {
-        const uint32_t hn = h ^ 1u;
+      const uint32_t g = es.nbox + c;
+      const uint32_t h = g & 3u;
+      if (c + WG_AHEAD < 8) {
+        const uint32_t hn = (g + WG_AHEAD) & 3u;
         if (lane == 0) {
-          bulk_wait_read0();  // the store that last used buffer hn has read it
+          bulk_wait_read1();  // every store but the latest (box c - 1) has read its buffer
           const uint32_t bar = lbar + 8 * hn;
           mbar_expect_tx(bar, BOX_BYTES);
-          tma_load_2d(ebuf + hn * BOX_BYTES, wg_map, bar, t.n0 + (c + 1) * 32, wg_orow);
+          tma_load_2d(ebuf + hn * BOX_BYTES, wg_map, bar, t.n0 + (c + WG_AHEAD) * 32, wg_orow);
         }
         es.pending[hn] = true;
       }
@@ -430,6 +483,7 @@ __device__ __forceinline__ bool epilogue_tile(const TcMaps& maps, const TcArgs& 
       if (!mbar_wait(lbar + 8 * h, es.uses[h] & 1u, abort_flag, a.err, 501)) return false;
       ++es.uses[h];
       es.pending[h] = false;
+      const uint32_t buf = ebuf + h * BOX_BYTES;
       float old[32], v[32];
       box_get_f32x32(buf, lane, old);
 #pragma unroll
@@ -469,21 +523,25 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
   using Cfg = ModeCfg<MODE>;
   constexpr int NST = Cfg::NST;
   extern __shared__ uint8_t smem_raw[];
+  // the same offsets in both CTAs of the pair: the MMA reads both at these addresses
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ctrl = smem + Cfg::CTRL_OFF;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(ctrl);        // [NST]
-  uint64_t* empty_bar = full_bar + 4;                             // [NST]
-  uint64_t* tfull_bar = empty_bar + 4;                            // [2]
-  uint64_t* tempty_bar = tfull_bar + 2;                           // [2]
-  uint64_t* drain_bar = tempty_bar + 2;                           // [1]
-  uint64_t* load_bar = drain_bar + 1;                             // [EPI_WARPS][2] (dgrad h inputs)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(load_bar + 2 * EPI_WARPS);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(ctrl);  // [MAX_ST] (used in the first CTA)
+  uint64_t* empty_bar = full_bar + MAX_ST;                  // [MAX_ST]
+  uint64_t* tfull_bar = empty_bar + MAX_ST;                 // [2]
+  uint64_t* tempty_bar = tfull_bar + 2;                     // [2] (used in the first CTA)
+  uint64_t* drain_bar = tempty_bar + 2;                     // [1]
+  uint64_t* load_bar = drain_bar + 1;                       // [EPI_WARPS][4] (dgrad h, wgrad inputs)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(load_bar + 4 * EPI_WARPS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_total = reinterpret_cast<int*>(tmem_slot + 2);
-  int* s_off = reinterpret_cast<int*>(ctrl + 256);  // E + 1 ints
+  int* s_off = reinterpret_cast<int*>(ctrl + 320);  // E + 1 ints
   int* s_cnt = s_off + MAX_E + 1;                   // E ints
+  int* s_pair = s_cnt + MAX_E;                      // E + 1 ints
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs of the pair
+  const int pair = blockIdx.x / 2, npairs = gridDim.x / 2;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
@@ -492,35 +550,46 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_addr(&tfull_bar[i]), 1);
-      mbar_init(smem_addr(&tempty_bar[i]), EPI_WARPS);
+      mbar_init(smem_addr(&tempty_bar[i]), 2 * EPI_WARPS);
     }
     mbar_init(smem_addr(drain_bar), 1);
-    for (int i = 0; i < 2 * EPI_WARPS; ++i) mbar_init(smem_addr(&load_bar[i]), 1);
+    for (int i = 0; i < 4 * EPI_WARPS; ++i) mbar_init(smem_addr(&load_bar[i]), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   for (int i = threadIdx.x; i <= a.E; i += THREADS) s_off[i] = a.offsets[i];
   for (int i = threadIdx.x; i < a.E; i += THREADS) s_cnt[i] = a.counts[i];
+  __syncthreads();
+  cluster_sync();  // the peer's barriers exist before any arrival crosses the pair
   if (warp == 1) {
-    tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_addr(tmem_slot), TMEM_COLS);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // both TMEM bases written
   tc_fence_after();
   if (threadIdx.x == 0) {
+    // both CTAs must see one TMEM base: the MMA writes the same columns in both
+    const uint32_t other = ld_shared_cluster_u32(mapa_shared(smem_addr(tmem_slot), rank ^ 1u));
+    const bool same_tmem = other == *tmem_slot;
+    if (!same_tmem) report_error(a.err, DEV_BAD_OFFSETS, 60 + MODE);
     // validate the routing state before trusting it for addresses
-    bool ok = s_off[0] == 0 && (int64_t)s_off[a.E] <= a.max_rows;
+    bool ok = s_off[0] == 0 && (int64_t)s_off[a.E] <= a.max_rows && (s_off[a.E] & (BM - 1)) == 0;
     for (int e = 0; e < a.E && ok; ++e) {
       const int len = s_off[e + 1] - s_off[e];
       ok = len >= 0 && (s_off[e] & (BM - 1)) == 0 && s_cnt[e] >= 0 && s_cnt[e] <= len;
     }
-    ok = ok && (s_off[a.E] & (BM - 1)) == 0;
     int total = 0;
-    if (ok) {
-      if (MODE == M_WGRAD) total = a.E * 3 * (a.d / BM) * (a.f / BN);
-      else total = (s_off[a.E] / BM) * n_tiles_of<MODE>(a);
-    } else if (blockIdx.x == 0) {
+    if (ok && same_tmem) {
+      if (MODE == M_WGRAD) {
+        total = a.E * 3 * (a.d / (2 * BM)) * (a.f / BN);
+      } else {
+        s_pair[0] = 0;
+        for (int e = 0; e < a.E; ++e) s_pair[e + 1] = s_pair[e] + ((s_off[e + 1] - s_off[e]) / BM + 1) / 2;
+        total = s_pair[a.E] * n_tiles_of<MODE>(a);
+      }
+    } else if (!ok && blockIdx.x == 0) {
       report_error(a.err, DEV_BAD_OFFSETS, 30 + MODE);
     }
     *s_total = total;
@@ -532,24 +601,25 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer ----------------
+      // ---------------- TMA producer (both CTAs) ----------------
       constexpr int NLOAD = MODE == M_UP ? 3 : (MODE == M_DGRAD_X ? 4 : (MODE == M_WGRAD ? 5 : 2));
       for (int i = 0; i < NLOAD; ++i) prefetch_map(&maps.m[i]);
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
       bool alive = true;
-      for (int tile = blockIdx.x; tile < total && alive; tile += gridDim.x) {
-        const Tile t = decode<MODE>(tile, a, s_off, s_cnt);
+      for (int tile = pair; tile < total && alive; tile += npairs) {
+        const Tile t = decode<MODE>(tile, rank, a, s_off, s_cnt, s_pair);
         for (int kb = 0; kb < t.kblocks; ++kb) {
           if (!mbar_wait(smem_addr(&empty_bar[stage]), phase ^ 1u, abort_flag, a.err, 100 + MODE)) {
             alive = false;
             break;
           }
-          const uint32_t fb = smem_addr(&full_bar[stage]);
-          mbar_expect_tx(fb, STAGE_BYTES);
+          const uint32_t fb_local = smem_addr(&full_bar[stage]);
+          if (rank == 0) mbar_expect_tx(fb_local, PAIR_STAGE_BYTES);
+          const uint32_t fb = rank == 0 ? fb_local : mapa_shared(fb_local, 0);
           const uint32_t sA = smem_base + stage * STAGE_BYTES;
-          issue_stage<MODE>(maps, a, t, kb, sA, sA + A_BYTES, fb);
+          issue_stage<MODE>(maps, a, t, kb, sA, sA + A_BYTES, fb, rank);
           ++issued;
           if (++stage == NST) {
             stage = 0;
@@ -558,24 +628,32 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
         }
       }
       if (!alive) {
-        // drain the copies still in flight before the CTA may exit
-        const int n = issued < NST ? issued : NST;
-        int s = stage;
-        uint32_t ph = phase;
-        for (int i = 0; i < n; ++i) {
-          if (--s < 0) {
-            s = NST - 1;
-            ph ^= 1u;
+        // drain the copies still in flight before the CTA may exit: the first
+        // CTA watches its full barriers; the second, whose copies complete on
+        // the first CTA's barriers, gives its copies a bounded 20 ms
+        if (rank == 0) {
+          const int n = issued < NST ? issued : NST;
+          int s = stage;
+          uint32_t ph = phase;
+          for (int i = 0; i < n; ++i) {
+            if (--s < 0) {
+              s = NST - 1;
+              ph ^= 1u;
+            }
+            const uint32_t fb = smem_addr(&full_bar[s]);
+            for (uint32_t it = 0; it < (1u << 24) && !mbar_try_wait(fb, ph); ++it) {
+            }
           }
-          const uint32_t fb = smem_addr(&full_bar[s]);
-          for (uint32_t it = 0; it < (1u << 24) && !mbar_try_wait(fb, ph); ++it) {
+        } else if (issued > 0) {
+          const uint64_t t0 = globaltimer();
+          while (globaltimer() - t0 < 20000000ull) {
           }
         }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer ----------------
+    if (lane == 0 && rank == 0) {
+      // ---------------- MMA issuer (first CTA of the pair) ----------------
       constexpr bool A_MN = MODE == M_WGRAD;
       constexpr bool B_MN = MODE == M_UP || MODE == M_DOWN || MODE == M_WGRAD;
       constexpr uint32_t IDESC = idesc_bf16(A_MN, B_MN);
@@ -583,10 +661,10 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
       uint32_t phase = 0;
       int local = 0;
       bool alive = true;
-      for (int tile = blockIdx.x; tile < total && alive; tile += gridDim.x, ++local) {
-        const Tile t = decode<MODE>(tile, a, s_off, s_cnt);
-        const int acc = local & 1;
-        const uint32_t use = (uint32_t)(local >> 1) & 1u;
+      for (int tile = pair; tile < total && alive; tile += npairs, ++local) {
+        const Tile t = decode<MODE>(tile, rank, a, s_off, s_cnt, s_pair);
+        const int acc = local % ACC_BUFS;
+        const uint32_t use = (uint32_t)(local / ACC_BUFS) & 1u;
         if (!mbar_wait(smem_addr(&tempty_bar[acc]), use ^ 1u, abort_flag, a.err, 200 + MODE)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
@@ -602,44 +680,50 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
           for (int k16 = 0; k16 < BK / 16; ++k16) {
             const uint64_t ad = A_MN ? sdesc(sA + k16 * 2048, 8192, 1024) : sdesc(sA + k16 * 32, 16, 1024);
             const uint64_t bd = B_MN ? sdesc(sB + k16 * 2048, 8192, 1024) : sdesc(sB + k16 * 32, 16, 1024);
-            umma_bf16(d_tmem, ad, bd, IDESC, (kb | k16) != 0 ? 1u : 0u);
+            umma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | k16) != 0 ? 1u : 0u);
           }
-          umma_commit(smem_addr(&empty_bar[stage]));
+          umma_commit_pair(smem_addr(&empty_bar[stage]), 0x3);
           if (++stage == NST) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!alive) break;
-        umma_commit(smem_addr(&tfull_bar[acc]));
+        umma_commit_pair(smem_addr(&tfull_bar[acc]), 0x3);
       }
-      // all MMAs of this thread complete before TMEM can be released
-      umma_commit(smem_addr(drain_bar));
+      // all MMAs of the pair complete (in both CTAs' TMEM) before TMEM is released
+      if (total > 0) umma_commit_pair(smem_addr(drain_bar), 0x3);
+    }
+    if (lane == 0 && total > 0) {
       for (uint32_t it = 0; it < (1u << 26) && !mbar_try_wait(smem_addr(drain_bar), 0); ++it) {
       }
     }
   } else {
-    // ---------------- epilogue warps 2..5 ----------------
+    // ---------------- epilogue warps 2..5 (both CTAs) ----------------
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int ew = warp - 2;
     const uint32_t ebuf = smem_base + Cfg::EPI_OFF + ew * Cfg::EPI_WARP_BYTES;
-    const uint32_t lbar = smem_addr(&load_bar[2 * ew]);
-    EpiState es{0u, {0u, 0u}, {false, false}};
+    const uint32_t lbar = smem_addr(&load_bar[4 * ew]);
+    EpiState es{0u, {0u, 0u, 0u, 0u}, {false, false, false, false}};
     int local = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
-      const Tile t = decode<MODE>(tile, a, s_off, s_cnt);
-      const int acc = local & 1;
-      const uint32_t use = (uint32_t)(local >> 1) & 1u;
+    for (int tile = pair; tile < total; tile += npairs, ++local) {
+      const Tile t = decode<MODE>(tile, rank, a, s_off, s_cnt, s_pair);
+      const int acc = local % ACC_BUFS;
+      const uint32_t use = (uint32_t)(local / ACC_BUFS) & 1u;
       const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
       if (!epilogue_tile<MODE>(maps, a, t, tacc, q, lane, ebuf, lbar, es, smem_addr(&tfull_bar[acc]), use,
                                abort_flag))
         break;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&tempty_bar[acc]));
+      if (lane == 0) {
+        const uint32_t te = smem_addr(&tempty_bar[acc]);
+        if (rank == 0) mbar_arrive(te);
+        else mbar_arrive_cluster(mapa_shared(te, 0));
+      }
     }
     // input loads still in flight (only after an abort), then every store
-    for (int h = 0; h < 2; ++h)
+    for (int h = 0; h < 4; ++h)
       if (es.pending[h])
         for (uint32_t it = 0; it < (1u << 24) && !mbar_try_wait(lbar + 8 * h, es.uses[h] & 1u); ++it) {
         }
@@ -649,8 +733,9 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still touch its barriers, operands or TMEM
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+  if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
 // ------------------------------ host side --------------------------------- //
@@ -697,8 +782,26 @@ int num_sms() {
   return cached[dev];
 }
 
+// Clusters of two resident at once for this kernel (one CTA per SM).
 template <int MODE>
-cudaError_t launch_mode(const TcMaps& maps, const TcArgs& args, int64_t tile_bound, int kind, cudaStream_t st) {
+int max_pairs(cudaLaunchConfig_t cfg) {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<MODE>, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = num_sms() / 2;
+    }
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+template <int MODE>
+cudaError_t launch_mode(const TcMaps& maps, const TcArgs& args, int64_t pair_bound, int kind, cudaStream_t st) {
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -709,11 +812,23 @@ cudaError_t launch_mode(const TcMaps& maps, const TcArgs& args, int64_t tile_bou
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  if (tile_bound <= 0) return cudaSuccess;
-  const int grid = (int)(tile_bound < num_sms() ? tile_bound : num_sms());
+  if (pair_bound <= 0) return cudaSuccess;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = ModeCfg<MODE>::SMEM;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(2);
+  const int64_t pairs = std::min<int64_t>(pair_bound, max_pairs<MODE>(cfg));
+  cfg.gridDim = dim3((unsigned)(2 * pairs));
   LaunchScope ls(kind, st);
-  tc_gemm_kernel<MODE><<<grid, THREADS, ModeCfg<MODE>::SMEM, st>>>(maps, args);
-  return cudaGetLastError();
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<MODE>, maps, args);
 }
 
 }  // namespace
@@ -740,15 +855,15 @@ cudaError_t tc_ffn_fwd(const Shape& s, const FfnFwdArgs& f, uint32_t* err, cudaS
   ok = ok && make_map(&down.m[0], f.h, R, ff, 64, BM) && make_map(&down.m[1], f.W2, E * ff, d, 64, 64) &&
        make_map(&down.m[2], f.y_perm, R, d, 64, 32);
   if (!ok) return cudaErrorInvalidValue;
-  const int64_t mt = s.max_rows / BM;
+  const int64_t mp = (s.max_rows / BM + s.E + 1) / 2;  // bound on pair tiles of 2 x 128 rows
   a.o0 = static_cast<__nv_bfloat16*>(f.h);
   a.o1 = static_cast<__nv_bfloat16*>(f.a);
   a.o2 = static_cast<__nv_bfloat16*>(f.b);
-  cudaError_t e = launch_mode<M_UP>(up, a, mt * (s.f / 128), KK_GEMM_UP, st);
+  cudaError_t e = launch_mode<M_UP>(up, a, mp * (s.f / 128), KK_GEMM_UP, st);
   if (e != cudaSuccess) return e;
   a.o0 = static_cast<__nv_bfloat16*>(f.y_perm);
   a.o1 = a.o2 = nullptr;
-  return launch_mode<M_DOWN>(down, a, mt * (s.d / BN), KK_GEMM_DOWN, st);
+  return launch_mode<M_DOWN>(down, a, mp * (s.d / BN), KK_GEMM_DOWN, st);
 }
 
 cudaError_t tc_ffn_bwd(const Shape& s, const FfnBwdArgs& b, uint32_t* err, cudaStream_t st) {
@@ -772,7 +887,7 @@ cudaError_t tc_ffn_bwd(const Shape& s, const FfnBwdArgs& b, uint32_t* err, cudaS
   a.err = err;
   a.accumulate = b.accumulate;
   TcMaps mh{}, mw{}, mx{};
-  bool ok = make_map(&mh.m[0], b.dy_perm, R, d, 64, BM) && make_map(&mh.m[1], b.W2, E * ff, d, 64, BN) &&
+  bool ok = make_map(&mh.m[0], b.dy_perm, R, d, 64, BM) && make_map(&mh.m[1], b.W2, E * ff, d, 64, BNH) &&
             make_map(&mh.m[2], b.a, R, ff, 64, 32) && make_map(&mh.m[3], b.b, R, ff, 64, 32) &&
             make_map(&mh.m[4], b.da, R, ff, 64, 32) && make_map(&mh.m[5], b.db, R, ff, 64, 32);
   ok = ok && make_map(&mw.m[0], b.x_perm, R, d, 64, 64) && make_map(&mw.m[1], b.h, R, ff, 64, 64) &&
@@ -780,24 +895,24 @@ cudaError_t tc_ffn_bwd(const Shape& s, const FfnBwdArgs& b, uint32_t* err, cudaS
        make_map(&mw.m[4], b.dy_perm, R, d, 64, 64) && make_map(&mw.m[5], b.dW1, E * d, ff, 32, 32, true) &&
        make_map(&mw.m[6], b.dW3, E * d, ff, 32, 32, true) && make_map(&mw.m[7], b.dW2, E * ff, d, 32, 32, true);
   ok = ok && make_map(&mx.m[0], b.da, R, ff, 64, BM) && make_map(&mx.m[1], b.db, R, ff, 64, BM) &&
-       make_map(&mx.m[2], b.W1, E * d, ff, 64, BN) && make_map(&mx.m[3], b.W3, E * d, ff, 64, BN) &&
+       make_map(&mx.m[2], b.W1, E * d, ff, 64, BNH) && make_map(&mx.m[3], b.W3, E * d, ff, 64, BNH) &&
        make_map(&mx.m[4], b.dx_perm, R, d, 64, 32);
   if (!ok) return cudaErrorInvalidValue;
-  const int64_t mt = s.max_rows / BM;
+  const int64_t mp = (s.max_rows / BM + s.E + 1) / 2;
   a.o0 = static_cast<__nv_bfloat16*>(b.da);
   a.o1 = static_cast<__nv_bfloat16*>(b.db);
   a.i0 = static_cast<const __nv_bfloat16*>(b.a);
   a.i1 = static_cast<const __nv_bfloat16*>(b.b);
-  cudaError_t e = launch_mode<M_DGRAD_H>(mh, a, mt * (s.f / BN), KK_GEMM_DGRAD_H, st);
+  cudaError_t e = launch_mode<M_DGRAD_H>(mh, a, mp * (s.f / BN), KK_GEMM_DGRAD_H, st);
   if (e != cudaSuccess) return e;
   a.w0 = b.dW1;
   a.w1 = b.dW3;
   a.w2 = b.dW2;
-  e = launch_mode<M_WGRAD>(mw, a, (int64_t)s.E * 3 * (s.d / BM) * (s.f / BN), KK_GEMM_WGRAD, st);
+  e = launch_mode<M_WGRAD>(mw, a, (int64_t)s.E * 3 * (s.d / (2 * BM)) * (s.f / BN), KK_GEMM_WGRAD, st);
   if (e != cudaSuccess) return e;
   a.o0 = static_cast<__nv_bfloat16*>(b.dx_perm);
   a.o1 = nullptr;
-  return launch_mode<M_DGRAD_X>(mx, a, mt * (s.d / BN), KK_GEMM_DGRAD_X, st);
+  return launch_mode<M_DGRAD_X>(mx, a, mp * (s.d / BN), KK_GEMM_DGRAD_X, st);
 }
 
 }  // namespace moe
