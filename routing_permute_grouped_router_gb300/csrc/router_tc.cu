@@ -11,10 +11,15 @@
 // MMAs per K step give fp32-accurate logits while reading x from HBM once at
 // TMA speed.
 //
-// One CTA per 128-token tile: warp 0 lane 0 loads 128x64 x tiles and the three
-// E_pad x 64 weight tiles with TMA, warp 1 lane 0 issues tcgen05.mma
-// (M=128, N=E_pad, K=16) into an fp32 TMEM accumulator, and warps 2-5 read one
-// token row per thread from TMEM and do softmax and top-k in registers (value
+// One cluster of cs CTAs per 128-token tile, CTA r of the cluster taking the
+// r-th of cs equal K ranges (cs = 1, 2, 4 or 8, the largest that keeps tiles x
+// cs within the SM count, so that few tokens still spread over the GPU): warp
+// 0 lane 0 loads 128x64 x tiles and the three E_pad x 64 weight tiles with
+// TMA, warp 1 lane 0 issues tcgen05.mma (M=128, N=E_pad, K=16) into an fp32
+// TMEM accumulator, and warps 2-5 read one token row per thread from TMEM.
+// CTAs r > 0 park their partial logits in their shared memory; the first CTA
+// adds them over distributed shared memory in rank order (so the sum does not
+// depend on timing) and does softmax and top-k in registers (value
 // descending, lower expert index on ties).  The histogram is written per
 // 64-token block, the layout the slot scan reads.
 #include <cudaTypedefs.h>
@@ -31,6 +36,7 @@ constexpr int RK = 64;   // K per stage (128-byte rows)
 constexpr int HIST_TOK = 64;
 constexpr int R_THREADS = 192;
 constexpr int R_MAXK = 8;
+constexpr int MAX_CS = 8;  // K ranges (cluster size) per token tile
 
 template <int N>
 struct RCfg {
@@ -42,6 +48,7 @@ struct RCfg {
   static constexpr int CTRL_OFF = NST * STAGE;
   static constexpr int SMEM = CTRL_OFF + 256 + 1024;
   static constexpr uint32_t TCOLS = N < 32 ? 32 : N;
+  static_assert(RT * (N + 4) * 4 <= NST * STAGE, "partial logits fit in the stage buffers");
   // fp32 D, bf16 A and B, both K-major, M = 128, N
   static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
                                     ((uint32_t)(RT >> 4) << 24);
@@ -80,6 +87,7 @@ __global__ void __launch_bounds__(R_THREADS, 1) router_tc_kernel(const __grid_co
                                                                  const __grid_constant__ CUtensorMap map_w,
                                                                  const __grid_constant__ RouterTcArgs a) {
   using C = RCfg<N>;
+  constexpr int PSTRIDE = N + 4;  // floats per parked row (16-byte rows, no bank conflicts)
   extern __shared__ uint8_t smem_raw[];
   __shared__ int hist_s[2][R_MAXK][N];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -91,7 +99,8 @@ __global__ void __launch_bounds__(R_THREADS, 1) router_tc_kernel(const __grid_co
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int tile = blockIdx.x;
+  const uint32_t cs = cluster_nctarank(), rank = cluster_ctarank();
+  const int tile = blockIdx.x / (int)cs;
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NST; ++i) {
       mbar_init(smem_addr(&full_bar[i]), 1);
@@ -100,7 +109,7 @@ __global__ void __launch_bounds__(R_THREADS, 1) router_tc_kernel(const __grid_co
     mbar_init(smem_addr(tfull_bar), 1);
     mbar_init(smem_addr(drain_bar), 1);
     *abort_flag = 0;
-    if (tile == 0) *a.ticket = 0;  // for the last-block election of the slot scan
+    if (tile == 0 && rank == 0) *a.ticket = 0;  // for the last-block election of the slot scan
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   for (int i = threadIdx.x; i < 2 * R_MAXK * N; i += R_THREADS) (&hist_s[0][0][0])[i] = 0;
@@ -113,7 +122,11 @@ __global__ void __launch_bounds__(R_THREADS, 1) router_tc_kernel(const __grid_co
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const uint32_t smem_base = smem_addr(smem);
-  const int kblocks = a.d / RK;
+  const int kall = a.d / RK;
+  const int kb0 = (int)rank * kall / (int)cs, kb1 = ((int)rank + 1) * kall / (int)cs;
+  const int kblocks = kb1 - kb0;
+  float v[N];  // this thread's token row of logits (epilogue warps)
+  bool have = false;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -130,9 +143,9 @@ __global__ void __launch_bounds__(R_THREADS, 1) router_tc_kernel(const __grid_co
         const uint32_t fb = smem_addr(&full_bar[stage]);
         mbar_expect_tx(fb, C::STAGE);
         const uint32_t sA = smem_base + stage * C::STAGE;
-        tma_load_2d(sA, &map_x, fb, kb * RK, tile * RT);
+        tma_load_2d(sA, &map_x, fb, (kb0 + kb) * RK, tile * RT);
 #pragma unroll
-        for (int s = 0; s < 3; ++s) tma_load_2d(sA + C::A_BYTES + s * N * 128, &map_w, fb, kb * RK, s * N);
+        for (int s = 0; s < 3; ++s) tma_load_2d(sA + C::A_BYTES + s * N * 128, &map_w, fb, (kb0 + kb) * RK, s * N);
         ++issued;
         if (++stage == C::NST) {
           stage = 0;
@@ -186,13 +199,10 @@ __global__ void __launch_bounds__(R_THREADS, 1) router_tc_kernel(const __grid_co
       }
     }
   } else {
-    // ---- epilogue: one token per thread ----
+    // ---- epilogue: one token row per thread ----
     const int q = warp & 3;
-    const int row = q * 32 + lane;
-    const int t = tile * RT + row;
     if (mbar_wait(smem_addr(tfull_bar), 0, abort_flag, a.err, 602)) {
       tc_fence_after();
-      float v[N];
 #pragma unroll
       for (int c = 0; c < N / 16; ++c) {
         uint32_t r[16];
@@ -201,92 +211,124 @@ __global__ void __launch_bounds__(R_THREADS, 1) router_tc_kernel(const __grid_co
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[c * 16 + i] = __uint_as_float(r[i]);
       }
-      if (t < a.T) {
-        float mx = -INFINITY;
+      have = true;
+      if (rank != 0) {
+        // the stage buffers are free once every MMA has completed
+        float4* prow = reinterpret_cast<float4*>(smem + (size_t)(q * 32 + lane) * PSTRIDE * 4);
 #pragma unroll
-        for (int e = 0; e < N; ++e) {
-          float l = -INFINITY;
-          if (e < a.E) {
-            l = v[e] + (a.bias != nullptr ? __ldg(a.bias + e) : 0.f);
-            if (isnan(l)) l = -INFINITY;
-          }
-          v[e] = l;
-          mx = fmaxf(mx, l);
-        }
-        float se = 0.f;
-#pragma unroll
-        for (int e = 0; e < N; ++e)
-          if (e < a.E) se += expf(v[e] - mx);
-        if (a.probs != nullptr) {
-          float* pr = a.probs + (size_t)t * a.E;
-#pragma unroll
-          for (int e = 0; e < N; ++e)
-            if (e < a.E) pr[e] = expf(v[e] - mx) / se;
-        }
-        float lj[R_MAXK];
-        int ej[R_MAXK];
-#pragma unroll
-        for (int j = 0; j < R_MAXK; ++j) {
-          lj[j] = 0.f;
-          ej[j] = 0;
-          if (j < a.k) {
-            float bv = -INFINITY;
-            int be = -1;
-#pragma unroll
-            for (int e = 0; e < N; ++e)
-              if (e < a.E && (be < 0 || v[e] > bv)) {  // strict: the lower index wins ties
-                bv = v[e];
-                be = e;
-              }
-#pragma unroll
-            for (int e = 0; e < N; ++e)
-              if (e == be) v[e] = -INFINITY;
-            // a taken expert is -inf; if every remaining logit is -inf the
-            // lowest untaken index still has to be found
-            if (bv == -INFINITY) {
-              be = -1;
-              for (int e = 0; e < a.E && be < 0; ++e) {
-                bool used = false;
-                for (int jj = 0; jj < j; ++jj) used |= ej[jj] == e;
-                if (!used) be = e;
-              }
-            }
-            lj[j] = bv;
-            ej[j] = be;
-          }
-        }
-        float g[R_MAXK];
-        if (a.k == 1) {
-          g[0] = expf(lj[0] - mx) / se;
-        } else {
-          float den = 0.f;
-#pragma unroll
-          for (int j = 0; j < R_MAXK; ++j)
-            if (j < a.k) {
-              g[j] = expf(lj[j] - lj[0]);
-              den += g[j];
-            }
-#pragma unroll
-          for (int j = 0; j < R_MAXK; ++j)
-            if (j < a.k) g[j] = g[j] / den;
-        }
-        const int half = row / HIST_TOK;
-#pragma unroll
-        for (int j = 0; j < R_MAXK; ++j)
-          if (j < a.k) {
-            a.ids[(size_t)t * a.k + j] = ej[j];
-            a.gates[(size_t)t * a.k + j] = g[j];
-            atomicAdd(&hist_s[half][j][ej[j]], 1);
-          }
+        for (int c = 0; c < N / 4; ++c) prow[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
       }
     }
   }
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  if (cs > 1) cluster_sync();  // every partial of the tile is in place
+  if (warp >= 2 && rank == 0) {
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const int t = tile * RT + row;
+    if (cs > 1) {
+      // add the other ranks' partial logits, in rank order
+      const uint32_t off = smem_addr(smem) + (uint32_t)row * PSTRIDE * 4;
+      for (uint32_t r = 1; r < cs; ++r) {
+        const uint32_t src = mapa_shared(off, r);
+#pragma unroll
+        for (int c = 0; c < N / 4; ++c) {
+          const float4 p = ld_shared_cluster_f4(src + 16 * c);
+          v[4 * c] += p.x;
+          v[4 * c + 1] += p.y;
+          v[4 * c + 2] += p.z;
+          v[4 * c + 3] += p.w;
+        }
+      }
+    }
+    if (have && t < a.T) {
+      float mx = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < N; ++e) {
+        float l = -INFINITY;
+        if (e < a.E) {
+          l = v[e] + (a.bias != nullptr ? __ldg(a.bias + e) : 0.f);
+          if (isnan(l)) l = -INFINITY;
+        }
+        v[e] = l;
+        mx = fmaxf(mx, l);
+      }
+      float se = 0.f;
+#pragma unroll
+      for (int e = 0; e < N; ++e)
+        if (e < a.E) se += expf(v[e] - mx);
+      if (a.probs != nullptr) {
+        float* pr = a.probs + (size_t)t * a.E;
+#pragma unroll
+        for (int e = 0; e < N; ++e)
+          if (e < a.E) pr[e] = expf(v[e] - mx) / se;
+      }
+      float lj[R_MAXK];
+      int ej[R_MAXK];
+#pragma unroll
+      for (int j = 0; j < R_MAXK; ++j) {
+        lj[j] = 0.f;
+        ej[j] = 0;
+        if (j < a.k) {
+          float bv = -INFINITY;
+          int be = -1;
+#pragma unroll
+          for (int e = 0; e < N; ++e)
+            if (e < a.E && (be < 0 || v[e] > bv)) {  // strict: the lower index wins ties
+              bv = v[e];
+              be = e;
+            }
+#pragma unroll
+          for (int e = 0; e < N; ++e)
+            if (e == be) v[e] = -INFINITY;
+          // a taken expert is -inf; if every remaining logit is -inf the
+          // lowest untaken index still has to be found
+          if (bv == -INFINITY) {
+            be = -1;
+            for (int e = 0; e < a.E && be < 0; ++e) {
+              bool used = false;
+              for (int jj = 0; jj < j; ++jj) used |= ej[jj] == e;
+              if (!used) be = e;
+            }
+          }
+          lj[j] = bv;
+          ej[j] = be;
+        }
+      }
+      float g[R_MAXK];
+      if (a.k == 1) {
+        g[0] = expf(lj[0] - mx) / se;
+      } else {
+        float den = 0.f;
+#pragma unroll
+        for (int j = 0; j < R_MAXK; ++j)
+          if (j < a.k) {
+            g[j] = expf(lj[j] - lj[0]);
+            den += g[j];
+          }
+#pragma unroll
+        for (int j = 0; j < R_MAXK; ++j)
+          if (j < a.k) g[j] = g[j] / den;
+      }
+      const int half = row / HIST_TOK;
+#pragma unroll
+      for (int j = 0; j < R_MAXK; ++j)
+        if (j < a.k) {
+          a.ids[(size_t)t * a.k + j] = ej[j];
+          a.gates[(size_t)t * a.k + j] = g[j];
+          atomicAdd(&hist_s[half][j][ej[j]], 1);
+        }
+    }
+  }
+  if (cs > 1) cluster_sync();  // the first CTA has read every partial
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
   tc_fence_after();
   // histogram of the two 64-token blocks of this tile, laid out [e][j][block]
-  for (int i = threadIdx.x; i < 2 * a.k * a.E; i += R_THREADS) {
+  for (int i = threadIdx.x; i < 2 * a.k * a.E && rank == 0; i += R_THREADS) {
     const int half = i / (a.k * a.E), r = i % (a.k * a.E), j = r / a.E, e = r % a.E;
     const int b = tile * 2 + half;
     if (b < a.nb) a.hist[((size_t)e * a.k + j) * a.nb + b] = hist_s[half][j][e];
@@ -324,7 +366,7 @@ bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t col
 int padded_experts(int E) { return E <= 16 ? 16 : (E <= 32 ? 32 : (E <= 64 ? 64 : 128)); }
 
 template <int N>
-cudaError_t launch_n(const CUtensorMap& mx, const CUtensorMap& mw, const RouterTcArgs& args, int tiles,
+cudaError_t launch_n(const CUtensorMap& mx, const CUtensorMap& mw, const RouterTcArgs& args, int tiles, int cs,
                      cudaStream_t st) {
   static bool attr_done[64] = {false};
   int dev = 0;
@@ -336,9 +378,33 @@ cudaError_t launch_n(const CUtensorMap& mx, const CUtensorMap& mw, const RouterT
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)(tiles * cs));
+  cfg.blockDim = dim3(R_THREADS);
+  cfg.dynamicSmemBytes = RCfg<N>::SMEM;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   LaunchScope ls(KK_ROUTER, st);
-  router_tc_kernel<N><<<tiles, R_THREADS, RCfg<N>::SMEM, st>>>(mx, mw, args);
-  return cudaGetLastError();
+  return cudaLaunchKernelEx(&cfg, router_tc_kernel<N>, mx, mw, args);
+}
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 1;
+  }
+  return cached[dev];
 }
 
 }  // namespace
@@ -366,11 +432,15 @@ cudaError_t launch_router_tc(const Shape& s, const void* x, const float* W_r, co
     return cudaErrorInvalidValue;
   RouterTcArgs a{bias, ids, gates, probs, hist, ticket, err, s.T, s.d, s.E, s.k, router_blocks(s.T)};
   const int tiles = (s.T + RT - 1) / RT;
+  // K ranges per tile: the most (up to 8) that keep one CTA per SM and at
+  // least two k-blocks per range
+  int cs = 1;
+  while (cs < MAX_CS && tiles * cs * 2 <= sm_count() && s.d / RK >= 4 * cs) cs *= 2;
   switch (N) {
-    case 16: return launch_n<16>(mx, mw, a, tiles, st);
-    case 32: return launch_n<32>(mx, mw, a, tiles, st);
-    case 64: return launch_n<64>(mx, mw, a, tiles, st);
-    default: return launch_n<128>(mx, mw, a, tiles, st);
+    case 16: return launch_n<16>(mx, mw, a, tiles, cs, st);
+    case 32: return launch_n<32>(mx, mw, a, tiles, cs, st);
+    case 64: return launch_n<64>(mx, mw, a, tiles, cs, st);
+    default: return launch_n<128>(mx, mw, a, tiles, cs, st);
   }
 }
 
