@@ -1,5 +1,6 @@
 // Device helpers shared by the row-moving and routing kernels: element loads
-// for fp32/bf16 activations, 16-byte vector packing, and the error word.
+// for fp32/bf16 activations, 16-byte vector packing, the error word, and the
+// programmatic dependent launch every kernel of the layer uses.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -56,6 +57,38 @@ __device__ __forceinline__ uint4 pack(const float (&v)[4]) {
 
 __device__ __forceinline__ uint4 ldg16(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
 __device__ __forceinline__ void stg16(void* p, const uint4& v) { *reinterpret_cast<uint4*>(p) = v; }
+
+// Programmatic dependent launch.  Each kernel of the layer is launched with
+// launch_pdl, so it may begin while the previous kernel of the stream is still
+// running: it calls pdl_wait() before its first access to global memory or
+// TMEM (the wait returns once the previous kernel has completed and its writes
+// are visible, and that kernel waited for its own predecessor the same way),
+// then pdl_launch_dependents() so the next kernel's launch overlaps its own
+// tail.  Without a programmatic predecessor the wait returns at once.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_enter() {
+  pdl_wait();
+  pdl_launch_dependents();
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

@@ -56,6 +56,7 @@ __device__ int expert_of_row(const int32_t* offsets, int E, int64_t row) {
 
 template <int MODE>
 __global__ void __launch_bounds__(256) simt_gemm_kernel(SimtArgs p) {
+  pdl_enter();  // see pdl_wait: no global access before this
   constexpr bool DUAL = MODE == S_UP;
   __shared__ float As[16][64 + 4];
   __shared__ float Bs[16][64 + 4];
@@ -197,8 +198,7 @@ template <int MODE>
 cudaError_t launch_simt(const SimtArgs& a, dim3 grid, int kind, cudaStream_t st) {
   if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
   LaunchScope ls(kind, st);
-  simt_gemm_kernel<MODE><<<grid, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(simt_gemm_kernel<MODE>, grid, dim3(256), 0, st, a);
 }
 
 }  // namespace

@@ -557,6 +557,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  pdl_enter();  // no global memory or TMEM access above this line
   for (int i = threadIdx.x; i <= a.E; i += THREADS) s_off[i] = a.offsets[i];
   for (int i = threadIdx.x; i < a.E; i += THREADS) s_cnt[i] = a.counts[i];
   __syncthreads();
@@ -813,11 +814,13 @@ cudaError_t launch_mode(const TcMaps& maps, const TcArgs& args, int64_t pair_bou
     attr_done[dev] = true;
   }
   if (pair_bound <= 0) return cudaSuccess;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg{};
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = ModeCfg<MODE>::SMEM;
@@ -827,6 +830,7 @@ cudaError_t launch_mode(const TcMaps& maps, const TcArgs& args, int64_t pair_bou
   cfg.gridDim = dim3(2);
   const int64_t pairs = std::min<int64_t>(pair_bound, max_pairs<MODE>(cfg));
   cfg.gridDim = dim3((unsigned)(2 * pairs));
+  cfg.numAttrs = 2;
   LaunchScope ls(kind, st);
   return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<MODE>, maps, args);
 }

@@ -67,6 +67,7 @@ struct RouterTcArgs {
 
 // W_r [d, E] fp32 -> wsplit [3][N][d] bf16 (hi, mid, lo; rows e >= E are zero).
 __global__ void split_wr_kernel(const float* W_r, __nv_bfloat16* wsplit, int d, int E, int N) {
+  pdl_enter();  // see pdl_wait: no global access before this
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (int64_t)N * d) return;
   const int e = (int)(i / d), c = (int)(i % d);
@@ -109,10 +110,11 @@ __global__ void __launch_bounds__(R_THREADS, 1) router_tc_kernel(const __grid_co
     mbar_init(smem_addr(tfull_bar), 1);
     mbar_init(smem_addr(drain_bar), 1);
     *abort_flag = 0;
-    if (tile == 0 && rank == 0) *a.ticket = 0;  // for the last-block election of the slot scan
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   for (int i = threadIdx.x; i < 2 * R_MAXK * N; i += R_THREADS) (&hist_s[0][0][0])[i] = 0;
+  pdl_enter();  // no global memory or TMEM access above this line
+  if (threadIdx.x == 0 && tile == 0 && rank == 0) *a.ticket = 0;  // for the last-block election of the slot scan
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), C::TCOLS);
     tmem_relinquish();
@@ -378,18 +380,20 @@ cudaError_t launch_n(const CUtensorMap& mx, const CUtensorMap& mw, const RouterT
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)(tiles * cs));
   cfg.blockDim = dim3(R_THREADS);
   cfg.dynamicSmemBytes = RCfg<N>::SMEM;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   LaunchScope ls(KK_ROUTER, st);
   return cudaLaunchKernelEx(&cfg, router_tc_kernel<N>, mx, mw, args);
 }
@@ -421,9 +425,8 @@ cudaError_t launch_router_tc(const Shape& s, const void* x, const float* W_r, co
   {
     const int64_t n = (int64_t)N * s.d;
     LaunchScope ls(KK_SPLIT_WR, st);
-    split_wr_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(W_r, static_cast<__nv_bfloat16*>(wsplit), s.d,
-                                                                  s.E, N);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(split_wr_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, W_r,
+                               static_cast<__nv_bfloat16*>(wsplit), s.d, s.E, N);
     if (e != cudaSuccess) return e;
   }
   CUtensorMap mx, mw;

@@ -45,6 +45,7 @@ struct RouterArgs {
 
 template <int EP, typename Tx>
 __global__ void __launch_bounds__(RT_THREADS) router_topk_kernel(RouterArgs a) {
+  pdl_enter();  // see pdl_wait: no global access before this
   constexpr int NT_E = EP < 32 ? EP : 32;   // threads along experts
   constexpr int TN = EP / NT_E;             // experts per thread
   constexpr int NT_T = RT_THREADS / NT_E;   // threads along tokens
@@ -214,6 +215,7 @@ struct ScanArgs {
 };
 
 __global__ void __launch_bounds__(256) slot_scan_kernel(ScanArgs a) {
+  pdl_enter();  // see pdl_wait: no global access before this
   __shared__ int warp_sums[8];
   __shared__ int is_last;
   const int e = blockIdx.x, tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
@@ -276,6 +278,7 @@ struct AssignArgs {
 };
 
 __global__ void __launch_bounds__(RT_TOK) slot_assign_kernel(AssignArgs a) {
+  pdl_enter();  // see pdl_wait: no global access before this
   __shared__ int cnt0[128];
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
   const int b = blockIdx.x;
@@ -329,11 +332,8 @@ __global__ void __launch_bounds__(RT_TOK) slot_assign_kernel(AssignArgs a) {
 template <int EP>
 cudaError_t launch_router_ep(const Shape& s, const RouterArgs& ra, cudaStream_t st) {
   LaunchScope ls(KK_ROUTER, st);
-  if (s.bf16)
-    router_topk_kernel<EP, __nv_bfloat16><<<ra.nb, RT_THREADS, 0, st>>>(ra);
-  else
-    router_topk_kernel<EP, float><<<ra.nb, RT_THREADS, 0, st>>>(ra);
-  return cudaGetLastError();
+  if (s.bf16) return launch_pdl(router_topk_kernel<EP, __nv_bfloat16>, dim3(ra.nb), dim3(RT_THREADS), 0, st, ra);
+  return launch_pdl(router_topk_kernel<EP, float>, dim3(ra.nb), dim3(RT_THREADS), 0, st, ra);
 }
 
 }  // namespace
@@ -355,8 +355,7 @@ cudaError_t launch_slot_scan(const Shape& s, const int32_t* hist, int32_t* base,
                              int32_t* ticket, int32_t* counts, int32_t* offsets, uint32_t* err, cudaStream_t st) {
   ScanArgs a{hist, base, totals, ticket, counts, offsets, err, s.E, s.k * router_blocks(s.T), s.cap, s.max_rows};
   LaunchScope ls(KK_SLOT_SCAN, st);
-  slot_scan_kernel<<<s.E, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(slot_scan_kernel, dim3(s.E), dim3(256), 0, st, a);
 }
 
 cudaError_t launch_slot_assign(const Shape& s, const int32_t* ids, const int32_t* base, const int32_t* counts,
@@ -365,8 +364,7 @@ cudaError_t launch_slot_assign(const Shape& s, const int32_t* ids, const int32_t
   AssignArgs a{ids, base, counts, offsets, slot, row_of, src_token, err, s.T, s.E, s.k,
                router_blocks(s.T), s.cap, s.max_rows};
   LaunchScope ls(KK_SLOT_ASSIGN, st);
-  slot_assign_kernel<<<a.nb + s.E, RT_TOK, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(slot_assign_kernel, dim3(a.nb + s.E), dim3(RT_TOK), 0, st, a);
 }
 
 }  // namespace moe

@@ -70,6 +70,7 @@ struct PermArgs {
 
 template <int K>
 __global__ void __launch_bounds__(RW_WARPS * 32) permute_kernel(PermArgs a) {
+  pdl_enter();  // see pdl_wait: no global access before this
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if ((int)blockIdx.x >= a.token_blocks) {
     zero_pad_rows(a.counts, a.offsets, blockIdx.x - a.token_blocks, a.x_perm, a.nvec, a.max_rows, a.err, warp,
@@ -116,6 +117,7 @@ struct CombArgs {
 
 template <typename Tx, int K>
 __global__ void __launch_bounds__(RW_WARPS * 32) combine_kernel(CombArgs a) {
+  pdl_enter();  // see pdl_wait: no global access before this
   constexpr int VN = Vec<Tx>::N;
   constexpr int U = INFLIGHT / K > 0 ? INFLIGHT / K : 1;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -181,6 +183,7 @@ struct CombBwdArgs {
 
 template <typename Tx, int K>
 __global__ void __launch_bounds__(RW_WARPS * 32) combine_bwd_kernel(CombBwdArgs a) {
+  pdl_enter();  // see pdl_wait: no global access before this
   constexpr int VN = Vec<Tx>::N;
   constexpr int U = INFLIGHT / (K + 1) > 0 ? INFLIGHT / (K + 1) : 1;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -275,6 +278,7 @@ __global__ void __launch_bounds__(RW_WARPS * 32) combine_bwd_kernel(CombBwdArgs 
 // W_r^T (E x d) so the router's input gradient reads contiguous rows.
 // -------------------------------------------------------------------------- //
 __global__ void transpose_wr_kernel(const float* W_r, float* W_rT, int d, int E) {
+  pdl_enter();  // see pdl_wait: no global access before this
   __shared__ float tile[32][33];
   const int i0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
   for (int r = threadIdx.y; r < 32; r += 8) {
@@ -304,6 +308,7 @@ struct DxArgs {
 
 template <typename Tx, int K>
 __global__ void __launch_bounds__(RW_WARPS * 32) dx_router_kernel(DxArgs a) {
+  pdl_enter();  // see pdl_wait: no global access before this
   constexpr int VN = Vec<Tx>::N;
   constexpr int U = INFLIGHT / K > 0 ? INFLIGHT / K : 1;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -398,6 +403,7 @@ __device__ __forceinline__ float2 load_pair(const __nv_bfloat16* p) {
 
 template <typename Tx>
 __global__ void __launch_bounds__(256) dwr_partial_kernel(DwArgs a) {
+  pdl_enter();  // see pdl_wait: no global access before this
   extern __shared__ float dw_acc[];  // [warps][E][DW_STRIDE]
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
   const int i0 = blockIdx.x * DW_COLS, s = blockIdx.y;
@@ -455,6 +461,7 @@ __global__ void __launch_bounds__(256) dwr_partial_kernel(DwArgs a) {
 }
 
 __global__ void dwr_reduce_kernel(const float* partial, float* dW_r, int splits, int64_t n, int accumulate) {
+  pdl_enter();  // see pdl_wait: no global access before this
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
   float p = 0.f;
@@ -468,11 +475,10 @@ int row_vecs(const Shape& s) { return s.d * (s.bf16 ? 2 : 4) / 16; }
 // Dispatch a (dtype, k) templated row kernel; k ranges over 1..8.
 template <template <typename, int> class Kern, typename Args>
 cudaError_t launch_typed_k(const Shape& s, const Args& a, int grid, cudaStream_t st) {
-#define MOE_ROWS_CASE(KK)                                    \
-  case KK:                                                   \
-    if (s.bf16) Kern<__nv_bfloat16, KK>::launch(a, grid, st); \
-    else Kern<float, KK>::launch(a, grid, st);               \
-    break;
+#define MOE_ROWS_CASE(KK)                                           \
+  case KK:                                                          \
+    if (s.bf16) return Kern<__nv_bfloat16, KK>::launch(a, grid, st); \
+    return Kern<float, KK>::launch(a, grid, st);
   switch (s.k) {
     MOE_ROWS_CASE(1)
     MOE_ROWS_CASE(2)
@@ -485,31 +491,30 @@ cudaError_t launch_typed_k(const Shape& s, const Args& a, int grid, cudaStream_t
     default: return cudaErrorInvalidValue;
   }
 #undef MOE_ROWS_CASE
-  return cudaGetLastError();
 }
 
 template <typename Tx, int K>
 struct CombineL {
-  static void launch(const CombArgs& a, int grid, cudaStream_t st) {
-    combine_kernel<Tx, K><<<grid, RW_WARPS * 32, 0, st>>>(a);
+  static cudaError_t launch(const CombArgs& a, int grid, cudaStream_t st) {
+    return launch_pdl(combine_kernel<Tx, K>, dim3(grid), dim3(RW_WARPS * 32), 0, st, a);
   }
 };
 template <typename Tx, int K>
 struct CombineBwdL {
-  static void launch(const CombBwdArgs& a, int grid, cudaStream_t st) {
-    combine_bwd_kernel<Tx, K><<<grid, RW_WARPS * 32, 0, st>>>(a);
+  static cudaError_t launch(const CombBwdArgs& a, int grid, cudaStream_t st) {
+    return launch_pdl(combine_bwd_kernel<Tx, K>, dim3(grid), dim3(RW_WARPS * 32), 0, st, a);
   }
 };
 template <typename Tx, int K>
 struct DxL {
-  static void launch(const DxArgs& a, int grid, cudaStream_t st) {
-    dx_router_kernel<Tx, K><<<grid, RW_WARPS * 32, 0, st>>>(a);
+  static cudaError_t launch(const DxArgs& a, int grid, cudaStream_t st) {
+    return launch_pdl(dx_router_kernel<Tx, K>, dim3(grid), dim3(RW_WARPS * 32), 0, st, a);
   }
 };
 template <typename Tx, int K>
 struct PermuteL {  // byte copies: the element type does not matter
-  static void launch(const PermArgs& a, int grid, cudaStream_t st) {
-    permute_kernel<K><<<grid, RW_WARPS * 32, 0, st>>>(a);
+  static cudaError_t launch(const PermArgs& a, int grid, cudaStream_t st) {
+    return launch_pdl(permute_kernel<K>, dim3(grid), dim3(RW_WARPS * 32), 0, st, a);
   }
 };
 
@@ -549,8 +554,7 @@ cudaError_t launch_dx_router(const Shape& s, const void* dx_perm, const int32_t*
   {
     dim3 grid((s.d + 31) / 32, (s.E + 31) / 32);
     LaunchScope ls(KK_TRANSPOSE_WR, st);
-    transpose_wr_kernel<<<grid, dim3(32, 8), 0, st>>>(W_r, W_rT, s.d, s.E);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(transpose_wr_kernel, grid, dim3(32, 8), 0, st, W_r, W_rT, s.d, s.E);
     if (e != cudaSuccess) return e;
   }
   DxArgs a{static_cast<const char*>(dx_perm), row_of, dl, W_rT, static_cast<char*>(dx), err, s.T, s.E, s.d,
@@ -594,15 +598,14 @@ cudaError_t launch_dwr(const Shape& s, const void* x, const float* dl, float* pa
     }
     dim3 grid((s.d + DW_COLS - 1) / DW_COLS, splits);
     LaunchScope ls(KK_DWR, st);
-    if (s.bf16) dwr_partial_kernel<__nv_bfloat16><<<grid, warps * 32, smem, st>>>(a);
-    else dwr_partial_kernel<float><<<grid, warps * 32, smem, st>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = s.bf16 ? launch_pdl(dwr_partial_kernel<__nv_bfloat16>, grid, dim3(warps * 32), smem, st, a)
+                           : launch_pdl(dwr_partial_kernel<float>, grid, dim3(warps * 32), smem, st, a);
     if (e != cudaSuccess) return e;
   }
   const int64_t n = (int64_t)s.d * s.E;
   LaunchScope ls(KK_DWR_REDUCE, st);
-  dwr_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(partial, dW_r, splits, n, accumulate);
-  return cudaGetLastError();
+  return launch_pdl(dwr_reduce_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st,
+                    static_cast<const float*>(partial), dW_r, splits, n, accumulate);
 }
 
 cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t st) {
