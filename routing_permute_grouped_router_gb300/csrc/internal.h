@@ -27,6 +27,7 @@ enum KernelKind : int {
   KK_ZERO,
   KK_SPLIT_WR,
   KK_SELFTEST,
+  KK_SPLIT_DL,
   KK_COUNT
 };
 
@@ -92,6 +93,17 @@ cudaError_t launch_dx_router(const Shape& s, const void* dx_perm, const int32_t*
 cudaError_t launch_dwr(const Shape& s, const void* x, const float* dl, float* partial, float* dW_r, int accumulate,
                        cudaStream_t st);
 int dwr_splits(const Shape& s);  // token slices of the router-weight gradient (partial buffer [splits][d][E])
+// Adds the token-slice partials [splits][d][E] in slice order into dW_r (n = d * E).
+cudaError_t launch_dwr_reduce(const float* partial, float* dW_r, int splits, int64_t n, int accumulate,
+                              cudaStream_t st);
+
+// ---- dwr_tc.cu: the router-weight gradient on the tensor cores (bf16 layers) ----
+bool dwr_tc_supported(const Shape& s);
+int dwr_tc_ranges(const Shape& s);           // token ranges (partial buffer [ranges][d][E])
+size_t dwr_tc_split_bytes(const Shape& s);   // the bf16 parts of dl
+// partial[r] = x^T dl over token range r; dW_r is then formed by launch_dwr_reduce.
+cudaError_t launch_dwr_tc(const Shape& s, const void* x, const float* dl, void* dlsplit, float* partial,
+                          uint32_t* err, cudaStream_t st);
 cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t st);
 
 // ---- gemm_tc.cu (bf16, tcgen05) and gemm_simt.cu (fp32) ----

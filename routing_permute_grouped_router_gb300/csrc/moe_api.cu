@@ -77,7 +77,8 @@ cudaEvent_t pool_event() {
 const char* const kKernelNames[KK_COUNT] = {
     "router_topk",  "slot_scan",  "slot_assign",     "permute",      "gemm_up_swiglu", "gemm_down",
     "unpermute_combine", "combine_bwd", "gemm_dgrad_h_swiglu_bwd", "gemm_wgrad", "gemm_dgrad_x",
-    "transpose_wr", "dx_router",  "dwr",     "dwr_reduce",   "zero", "split_wr", "selftest_bounded_wait"};
+    "transpose_wr", "dx_router",  "dwr",     "dwr_reduce",   "zero", "split_wr", "selftest_bounded_wait",
+    "split_dl"};
 
 }  // namespace
 
@@ -188,6 +189,7 @@ struct FwdScratch {
 struct BwdScratch {
   void *dy_perm, *da, *db, *dx_perm;
   float *dg, *dl, *W_rT, *partial;
+  void* dlsplit;  // bf16 parts of dl for the tensor-core router-weight gradient
 };
 
 RoutingScratch carve_routing(Carver& c, const Shape& s) {
@@ -225,7 +227,9 @@ BwdScratch carve_bwd(Carver& c, const Shape& s) {
   b.dg = static_cast<float*>(c.take((size_t)s.T * s.k * 4));
   b.dl = static_cast<float*>(c.take((size_t)s.T * s.E * 4));
   b.W_rT = static_cast<float*>(c.take((size_t)s.E * s.d * 4));
-  b.partial = static_cast<float*>(c.take((size_t)dwr_splits(s) * s.d * s.E * 4));
+  const bool tc = dwr_tc_supported(s);
+  b.partial = static_cast<float*>(c.take((size_t)(tc ? dwr_tc_ranges(s) : dwr_splits(s)) * s.d * s.E * 4));
+  b.dlsplit = c.take(tc ? dwr_tc_split_bytes(s) : 0);
   return b;
 }
 size_t ws_bytes_for(const Shape& s, int training) {
@@ -284,7 +288,12 @@ moe_status do_dx_router(const Shape& s, const void* x, const void* dx_perm, cons
     return MOE_OK;
   }
   CUDA_TRY(launch_dx_router(s, dx_perm, row_of, dl, W_r, bs.W_rT, dx, err, st));
-  CUDA_TRY(launch_dwr(s, x, dl, bs.partial, dW_r, accumulate, st));
+  if (dwr_tc_supported(s)) {
+    CUDA_TRY(launch_dwr_tc(s, x, dl, bs.dlsplit, bs.partial, err, st));
+    CUDA_TRY(launch_dwr_reduce(bs.partial, dW_r, dwr_tc_ranges(s), (int64_t)s.d * s.E, accumulate, st));
+  } else {
+    CUDA_TRY(launch_dwr(s, x, dl, bs.partial, dW_r, accumulate, st));
+  }
   return MOE_OK;
 }
 

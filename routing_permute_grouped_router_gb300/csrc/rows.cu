@@ -602,10 +602,14 @@ cudaError_t launch_dwr(const Shape& s, const void* x, const float* dl, float* pa
                            : launch_pdl(dwr_partial_kernel<float>, grid, dim3(warps * 32), smem, st, a);
     if (e != cudaSuccess) return e;
   }
-  const int64_t n = (int64_t)s.d * s.E;
+  return launch_dwr_reduce(partial, dW_r, splits, (int64_t)s.d * s.E, accumulate, st);
+}
+
+cudaError_t launch_dwr_reduce(const float* partial, float* dW_r, int splits, int64_t n, int accumulate,
+                              cudaStream_t st) {
   LaunchScope ls(KK_DWR_REDUCE, st);
-  return launch_pdl(dwr_reduce_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st,
-                    static_cast<const float*>(partial), dW_r, splits, n, accumulate);
+  return launch_pdl(dwr_reduce_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, partial, dW_r, splits,
+                    n, accumulate);
 }
 
 cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t st) {
