@@ -40,8 +40,10 @@ constexpr int MAX_CS = 8;  // K ranges (cluster size) per token tile
 
 template <int N>
 struct RCfg {
-  // as many stages as fit in ~180 KB: small E leaves room for deep prefetch of x
-  static constexpr int NST = N <= 16 ? 8 : (N <= 32 ? 6 : (N <= 64 ? 4 : 3));
+  // stages: up to N = 32 two CTAs fit on an SM (shared memory and registers),
+  // so a large T runs in one wave
+  static constexpr int NST = N <= 16 ? 5 : (N <= 32 ? 3 : (N <= 64 ? 4 : 3));
+  static constexpr int MIN_BLOCKS = N <= 32 ? 2 : 1;
   static constexpr int A_BYTES = RT * RK * 2;
   static constexpr int B_BYTES = 3 * N * RK * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
@@ -84,7 +86,7 @@ __global__ void split_wr_kernel(const float* W_r, __nv_bfloat16* wsplit, int d, 
 }
 
 template <int N>
-__global__ void __launch_bounds__(R_THREADS, 1) router_tc_kernel(const __grid_constant__ CUtensorMap map_x,
+__global__ void __launch_bounds__(R_THREADS, RCfg<N>::MIN_BLOCKS) router_tc_kernel(const __grid_constant__ CUtensorMap map_x,
                                                                  const __grid_constant__ CUtensorMap map_w,
                                                                  const __grid_constant__ RouterTcArgs a) {
   using C = RCfg<N>;
@@ -127,6 +129,11 @@ __global__ void __launch_bounds__(R_THREADS, 1) router_tc_kernel(const __grid_co
   const int kall = a.d / RK;
   const int kb0 = (int)rank * kall / (int)cs, kb1 = ((int)rank + 1) * kall / (int)cs;
   const int kblocks = kb1 - kb0;
+  // Tiles start their K loop at different k-blocks, so CTAs running together
+  // read different parts of W_r instead of all loading the same boxes from the
+  // same L2 lines.  The order is fixed per tile, so the sums do not depend on
+  // timing.
+  const int rot = kblocks > 0 ? (int)(((unsigned)tile * 7u) % (unsigned)kblocks) : 0;
   float v[N];  // this thread's token row of logits (epilogue warps)
   bool have = false;
 
@@ -137,7 +144,8 @@ __global__ void __launch_bounds__(R_THREADS, 1) router_tc_kernel(const __grid_co
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       bool alive = true;
-      for (int kb = 0; kb < kblocks; ++kb) {
+      for (int i = 0; i < kblocks; ++i) {
+        const int kb = (i + rot) % kblocks;
         if (!mbar_wait(smem_addr(&empty_bar[stage]), phase ^ 1u, abort_flag, a.err, 600)) {
           alive = false;
           break;
@@ -173,7 +181,7 @@ __global__ void __launch_bounds__(R_THREADS, 1) router_tc_kernel(const __grid_co
       int stage = 0;
       uint32_t phase = 0;
       bool alive = true;
-      for (int kb = 0; kb < kblocks; ++kb) {
+      for (int i = 0; i < kblocks; ++i) {
         if (!mbar_wait(smem_addr(&full_bar[stage]), phase, abort_flag, a.err, 601)) {
           alive = false;
           break;
@@ -187,7 +195,7 @@ __global__ void __launch_bounds__(R_THREADS, 1) router_tc_kernel(const __grid_co
 #pragma unroll
           for (int s = 0; s < 3; ++s)
             umma_bf16(tmem_base, ad, sdesc(sB + s * N * 128 + k16 * 32, 16, 1024), C::IDESC,
-                      (kb | k16 | s) != 0 ? 1u : 0u);
+                      (i | k16 | s) != 0 ? 1u : 0u);
         }
         umma_commit(smem_addr(&empty_bar[stage]));
         if (++stage == C::NST) {
