@@ -151,7 +151,9 @@ moe_status moe_max_rows(const moe_config* cfg, int64_t* rows);
 /* Bytes of workspace that moe_layer_fwd (training = 0) or moe_layer_fwd and
  * moe_layer_bwd (training = 1) need.  The workspace holds the routing
  * histograms, the forward intermediates when no moe_saved is given, and the
- * backward scratch.  Host only. */
+ * backward scratch.  Host only; for bf16 layers the router-weight gradient's
+ * partial sums scale with the SM count of the current device, so ask with the
+ * device that will run the layer current. */
 moe_status moe_workspace_size(const moe_config* cfg, int training, size_t* bytes);
 
 /* Router scoring, softmax, top-k and capacity slotting (steps "the router
