@@ -39,7 +39,13 @@ design notes):
 6. expert FFN is SwiGLU without biases: (silu(x W1) * (x W3)) W2,
    silu(z) = z / (1 + exp(-z));
 7. the router bias is a fixed term (no gradient); gradients are summed (not
-   averaged) over micro-batches.
+   averaged) over micro-batches;
+8. the auxiliary load-balancing loss, which the tutorial's MoE configuration
+   example only names ("aux_loss coeff"), is taken in its usual expert-balance
+   form L = coeff * E * sum_e f_e * P_e, where f_e is the share of the T*k
+   assignments that chose expert e before the capacity drop (a count: no
+   gradient flows through it) and P_e the mean router probability of e; it is
+   off (coeff = 0) unless asked for.
 
 Data layout of the permutation map (the library's convention, adopted here so
 that row numbers compare exactly): each expert's rows start at a multiple of
@@ -297,13 +303,45 @@ def router_logit_grad(dg: np.ndarray, st) -> np.ndarray:
     return dl
 
 
-def backward(dy, x, W_r, W1, W3, W2, st) -> Dict[str, np.ndarray]:
-    """Layer backward from the saved routing state (no re-routing)."""
+def aux_loss(probs: np.ndarray, ids: np.ndarray, coeff: float):
+    """Auxiliary load-balancing loss and its logit gradient (reading 8).
+
+    f_e = #{(t, j): ids[t, j] = e} / (T k)      assignment share before the drop
+    P_e = (1/T) sum_t probs[t, e]              mean router probability
+    L   = coeff * E * sum_e f_e P_e
+    With p = softmax(l) per token, dP_e / dl[t, e'] = p[t, e] (delta_ee' - p[t, e']) / T, so
+    dL/dl[t, e'] = coeff * E / T * p[t, e'] * (f_e' - sum_e f_e p[t, e]).
+    Returns (L, dL/dl [T, E]).
+    """
+    p = np.asarray(probs, np.float64)
+    T, E = p.shape
+    k = ids.shape[1]
+    f = np.zeros(E)
+    for t in range(T):
+        for j in range(k):
+            f[int(ids[t, j])] += 1.0
+    f /= T * k
+    P = p.mean(axis=0)
+    loss = coeff * E * float(np.dot(f, P))
+    dl = np.zeros_like(p)
+    for t in range(T):
+        s = float(np.dot(f, p[t]))
+        dl[t] = coeff * E / T * p[t] * (f - s)
+    return loss, dl
+
+
+def backward(dy, x, W_r, W1, W3, W2, st, aux_coeff: float = 0.0) -> Dict[str, np.ndarray]:
+    """Layer backward from the saved routing state (no re-routing).  With
+    aux_coeff > 0 the auxiliary loss's logit gradient joins dl (reading 8)."""
     dy = np.asarray(dy, np.float64)
     x = np.asarray(x, np.float64)
     dYp, dg = combine_backward(dy, st)
     fb = ffn_backward(dYp, st, W1, W3, W2)
     dl = router_logit_grad(dg, st)
+    aux = None
+    if aux_coeff > 0:
+        aux, dl_aux = aux_loss(st["probs"], st["ids"], aux_coeff)
+        dl = dl + dl_aux
     row_of = st["row_of"]
     T, k = row_of.shape
     dx = dl @ np.asarray(W_r, np.float64).T
@@ -313,6 +351,8 @@ def backward(dy, x, W_r, W1, W3, W2, st) -> Dict[str, np.ndarray]:
             if r >= 0:
                 dx[t] += fb["dX_perm"][r]
     out = dict(dx=dx, dW_r=x.T @ dl, dl=dl, dg=dg, dY_perm=dYp)
+    if aux is not None:
+        out["aux_loss"] = aux
     out.update(fb)
     return out
 

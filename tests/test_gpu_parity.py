@@ -283,3 +283,27 @@ def test_bounded_wait_reports_timeout_and_gpu_stays_usable():
     assert (detail & 0xFFFFFF) == 700
     assert 0.04 < waited < 5.0
     test_layer_forward("top2_e8_small")
+
+
+@pytest.mark.parametrize("k", [1, 2])
+def test_permute_then_unpermute_is_identity_on_gpu(k):
+    """moe_permute followed by moe_unpermute_combine with gates summing to 1 in
+    powers of two (1, or 0.5 + 0.5) gives x back bit for bit: every token is kept
+    (dropless), each of its rows is an exact copy, and the fp32 sum of the
+    halves of a bf16 value is that value."""
+    s = LS(f"ident_k{k}", 777, 256, 256, 8, k, 0.0, W.BF16)
+    wl = W.make(s, seed=11, micro_batches=1, with_dy=False)
+    cfg = pkg.config_of(s)
+    L = layer.from_workload(wl, training=True)
+    x = wl.x[0].torch("cuda")
+    L.forward(x)
+    sv = L.saved
+    x_perm = torch.zeros(L.max_rows, s.d_model, dtype=torch.bfloat16, device="cuda")
+    pkg.moe_permute(cfg, x, sv["row_of"], sv["counts"], sv["offsets"], x_perm)
+    gates = torch.full((s.T, k), 1.0 / k, dtype=torch.float32, device="cuda")
+    y = torch.empty_like(x)
+    pkg.moe_unpermute_combine(cfg, x_perm, sv["row_of"], gates, y)
+    torch.cuda.synchronize()
+    check_no_device_error()
+    assert (sv["slot"] >= 0).all()
+    assert torch.equal(y, x)

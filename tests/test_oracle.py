@@ -289,6 +289,85 @@ def test_gradient_accumulation_sums_micro_batches():
 
 
 # --------------------------------------------------------------------------- #
+# Auxiliary load-balancing loss (reading 8: coeff * E * sum_e f_e P_e)
+# --------------------------------------------------------------------------- #
+def test_aux_loss_balanced_routing_is_the_coefficient_with_zero_gradient():
+    # uniform probabilities and an equal share of assignments per expert: f = P = 1/E,
+    # so L = coeff * E * E * (1/E)^2 = coeff, and no logit can lower it to first order
+    T, E, k, coeff = 12, 4, 2, 0.37
+    probs = np.full((T, E), 1.0 / E)
+    ids = np.array([[(2 * t) % E, (2 * t + 1) % E] for t in range(T)])
+    loss, dl = O.aux_loss(probs, ids, coeff)
+    assert abs(loss - coeff) < 1e-15
+    assert np.abs(dl).max() < 1e-15
+
+
+def test_aux_loss_collapsed_routing_is_coefficient_times_experts():
+    # every assignment and all probability on expert 0: f_0 = P_0 = 1, L = coeff * E
+    T, E, coeff = 5, 6, 0.01
+    probs = np.zeros((T, E))
+    probs[:, 0] = 1.0
+    loss, _ = O.aux_loss(probs, np.zeros((T, 1), dtype=np.int64), coeff)
+    assert abs(loss - coeff * E) < 1e-15
+
+
+def test_aux_loss_hand_computed_example():
+    # T = 2, E = 2, k = 1, both tokens pick expert 0: f = (1, 0);
+    # P = ((0.75 + 0.5) / 2, (0.25 + 0.5) / 2) = (0.625, 0.375); L = c * 2 * 0.625 = 1.25 c
+    probs = np.array([[0.75, 0.25], [0.5, 0.5]])
+    loss, dl = O.aux_loss(probs, np.array([[0], [0]]), 0.2)
+    assert abs(loss - 0.25) < 1e-15
+    # dl[t, e'] = c E / T p[t, e'] (f_e' - sum_e f_e p[t, e]): token 0: s = 0.75
+    np.testing.assert_allclose(dl[0], [0.2 * 0.75 * 0.25, 0.2 * 0.25 * -0.75], rtol=0, atol=1e-15)
+
+
+def test_aux_loss_gradient_matches_finite_differences():
+    rng = np.random.default_rng(77)
+    T, E, k, coeff = 9, 5, 2, 0.3
+    l = rng.standard_normal((T, E))
+    ids = np.argsort(-l, axis=1, kind="stable")[:, :k]
+
+    def L(logits):
+        return O.aux_loss(O.softmax(logits), ids, coeff)[0]
+
+    _, dl = O.aux_loss(O.softmax(l), ids, coeff)
+    h = 1e-6
+    for _ in range(5):
+        v = rng.standard_normal(l.shape)
+        fd = (L(l + h * v) - L(l - h * v)) / (2 * h)
+        assert abs(fd - float((dl * v).sum())) <= 1e-8, fd
+
+
+def test_backward_with_aux_loss_matches_finite_differences():
+    # total loss <dy, y> + L_aux as a function of W_r and x (routing fixed within h)
+    rng = np.random.default_rng(31)
+    T, d, f, E, k, C, coeff = 12, 6, 7, 4, 2, 5, 0.5
+    x, W_r, W1, W3, W2 = _rand_layer(rng, T, d, f, E)
+    l = x @ W_r
+    srt = -np.sort(-l, axis=1)
+    assert (srt[:, :-1] - srt[:, 1:]).min() > 1e-4
+    dy = rng.standard_normal((T, d))
+    st = O.forward(x, W_r, None, W1, W3, W2, k, C)
+    gr = O.backward(dy, x, W_r, W1, W3, W2, st, aux_coeff=coeff)
+    assert abs(gr["aux_loss"] - O.aux_loss(st["probs"], st["ids"], coeff)[0]) < 1e-15
+
+    def total(xx, wr):
+        s2 = O.forward(xx, wr, None, W1, W3, W2, k, C)
+        return float((s2["y"] * dy).sum()) + O.aux_loss(s2["probs"], s2["ids"], coeff)[0]
+
+    h = 1e-6
+    for name, base, g in (("W_r", W_r, gr["dW_r"]), ("x", x, gr["dx"])):
+        for _ in range(3):
+            v = rng.standard_normal(base.shape)
+            if name == "W_r":
+                fd = (total(x, W_r + h * v) - total(x, W_r - h * v)) / (2 * h)
+            else:
+                fd = (total(x + h * v, W_r) - total(x - h * v, W_r)) / (2 * h)
+            an = float((g * v).sum())
+            assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (name, fd, an)
+
+
+# --------------------------------------------------------------------------- #
 # Planted mistakes: each must be caught by one of the pins above
 # --------------------------------------------------------------------------- #
 def _pins_pass():
@@ -300,6 +379,9 @@ def _pins_pass():
         for k, C in [(1, 4), (2, 5)]:
             test_backward_matches_finite_differences(k, C)
         test_slots_brute_force(3)
+        test_aux_loss_balanced_routing_is_the_coefficient_with_zero_gradient()
+        test_aux_loss_hand_computed_example()
+        test_aux_loss_gradient_matches_finite_differences()
     except AssertionError:
         return False
     return True
@@ -307,7 +389,7 @@ def _pins_pass():
 
 @pytest.mark.parametrize("mutation", [
     "silu_is_sigmoid", "transposed_w2", "gate_not_renormalised", "second_choice_first",
-    "router_grad_sign", "missing_router_dx", "slot_off_by_one",
+    "router_grad_sign", "missing_router_dx", "slot_off_by_one", "aux_share_per_token", "aux_grad_sign",
 ])
 def test_planted_mistake_is_caught(monkeypatch, mutation):
     if mutation == "silu_is_sigmoid":
@@ -344,6 +426,21 @@ def test_planted_mistake_is_caught(monkeypatch, mutation):
             s, c = orig(ids, E, None if C is None else C + 1)
             return s, c
         monkeypatch.setattr(O, "assign_slots", bad)
+    elif mutation == "aux_grad_sign":
+        orig = O.aux_loss
+
+        def bad(probs, ids, coeff):
+            loss, dl = orig(probs, ids, coeff)
+            return loss, -dl
+        monkeypatch.setattr(O, "aux_loss", bad)
+    elif mutation == "aux_share_per_token":
+        orig = O.aux_loss
+
+        def bad(probs, ids, coeff):  # f_e divided by T instead of T k
+            k = ids.shape[1]
+            loss, dl = orig(probs, ids, coeff * k)
+            return loss, dl
+        monkeypatch.setattr(O, "aux_loss", bad)
     assert not _pins_pass(), mutation
 
 
