@@ -47,6 +47,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--aux-loss-coeff", type=float, default=0.0,
+                   help="auxiliary load-balancing loss coefficient (the layer configurations use none)")
     return p.parse_args()
 
 
@@ -306,7 +308,7 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     s = W.WORKLOADS[args.workload]
     wl = W.make(s, seed=rank, micro_batches=1, with_dy=True)
-    L = layer.from_workload(wl, str(dev))
+    L = layer.from_workload(wl, str(dev), aux_loss_coeff=args.aux_loss_coeff)
     x = wl.x[0].torch(dev)
     dy = wl.dy[0].torch(dev)
     stream = torch.cuda.current_stream(dev)
@@ -477,7 +479,8 @@ def run_ours(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": s.dtype, "data": "synthetic",
         "config": {"workload": args.workload, "T": s.T, "d_model": s.d_model, "d_ff": s.d_ff, "E": s.E, "k": s.k,
-                   "capacity_factor": s.capacity_factor, "kept_assignments": N,
+                   "capacity_factor": s.capacity_factor, "aux_loss_coeff": args.aux_loss_coeff,
+                   "kept_assignments": N,
                    "step": "forward + backward (fp32 grad accumulate)",
                    "l2": "256 MB buffer written before every timed step, outside the step's events",
                    "parallelism": f"replicas x{world}",

@@ -93,6 +93,7 @@ typedef struct {
   float capacity_factor;    /* C = ceil(cf * T * k / E); <= 0 means dropless */
   int32_t capacity;         /* >= 0: use this exact capacity instead of the factor; < 0: use the factor */
   int32_t dtype;            /* moe_dtype of activations and expert weights */
+  float aux_loss_coeff;     /* >= 0; > 0 adds the auxiliary load-balancing loss to the backward (moe_aux_loss) */
 } moe_config;
 
 /* Expert and router parameters (device pointers, read only). */
@@ -132,6 +133,7 @@ typedef struct {
   float* dW1;
   float* dW3;
   float* dW2;
+  float* aux_loss;  /* device fp32 scalar that receives the auxiliary loss, or NULL */
 } moe_grads;
 
 /* Human-readable name of a status code (static storage). */
@@ -227,6 +229,23 @@ moe_status moe_grouped_ffn_bwd(const moe_config* cfg, const void* x_perm, const 
                                const void* W1, const void* W3, const void* W2, void* da, void* db, void* dx_perm,
                                float* dW1, float* dW3, float* dW2, int accumulate, moe_stream_t stream);
 
+/* Auxiliary load-balancing loss of the router and its logit gradient.  The
+ * tutorial's MoE configuration example names an "aux_loss" coefficient
+ * (distributed-training tutorial, "The Conflict Between EP and TP") without a
+ * formula; the usual expert-balance form is taken:
+ *   f_e = (assignments (t, j) with ids[t,j] = e, before the capacity drop) / (T k)
+ *   P_e = (1/T) sum_t probs[t,e]
+ *   L   = c * E * sum_e f_e P_e,          c = cfg->aux_loss_coeff
+ * f is a count and carries no gradient, so
+ *   dl[t,e'] += c * E / T * probs[t,e'] * (f_e' - sum_e f_e probs[t,e]).
+ * probs [T, E] fp32 and ids [T, k] int32 as moe_router_topk writes them; dl
+ * [T, E] fp32 is updated in place (moe_combine_bwd's output); *loss (device
+ * fp32, may be NULL) receives L.  Sums run in a fixed order (bitwise
+ * reproducible).  ws must hold moe_workspace_size(cfg, 1).  Does nothing when
+ * the coefficient is 0. */
+moe_status moe_aux_loss(const moe_config* cfg, const float* probs, const int32_t* ids, float* loss, float* dl,
+                        void* ws, size_t ws_bytes, moe_stream_t stream);
+
 /* Inverse permutation of the token gradient plus the router backward ("Its
  * gradient behaves like any other shared parameter", gpu_expert_parallel page):
  *   dx[t] = sum over kept j of dx_perm[row_of[t,j]] + dl[t] W_r^T
@@ -238,7 +257,9 @@ moe_status moe_unpermute_dx_router_bwd(const moe_config* cfg, const void* x, con
                                        moe_stream_t stream);
 
 /* Whole backward from the state saved by moe_layer_fwd (no re-routing):
- * moe_combine_bwd, moe_grouped_ffn_bwd, moe_unpermute_dx_router_bwd.
+ * moe_combine_bwd, moe_aux_loss (when cfg->aux_loss_coeff > 0; saved->probs is
+ * then required for every k and grads->aux_loss may receive the loss),
+ * moe_grouped_ffn_bwd, moe_unpermute_dx_router_bwd.
  * grads receives dW_r, dW1, dW3, dW2 (accumulate as above); dx [T, d] in dtype. */
 moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* w, const void* x, const void* dy,
                          const moe_saved* saved, void* dx, const moe_grads* grads, int accumulate, void* ws,

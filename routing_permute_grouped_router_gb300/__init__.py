@@ -35,7 +35,7 @@ class MoeError(RuntimeError):
 class MoeConfig(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("d_model", ctypes.c_int32), ("d_ff", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("capacity_factor", ctypes.c_float),
-                ("capacity", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+                ("capacity", ctypes.c_int32), ("dtype", ctypes.c_int32), ("aux_loss_coeff", ctypes.c_float)]
 
 
 class MoeWeights(ctypes.Structure):
@@ -49,7 +49,7 @@ class MoeSaved(ctypes.Structure):
 
 
 class MoeGrads(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_void_p) for n in ("dW_r", "dW1", "dW3", "dW2")]
+    _fields_ = [(n, ctypes.c_void_p) for n in ("dW_r", "dW1", "dW3", "dW2", "aux_loss")]
 
 
 _P = ctypes.c_void_p
@@ -71,6 +71,7 @@ _SIGNATURES = {
     "moe_combine_bwd": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_grouped_ffn_bwd": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P],
     "moe_unpermute_dx_router_bwd": [_CFG, _P, _P, _P, _P, _P, _P, _P, _I, _P, _Z, _P],
+    "moe_aux_loss": [_CFG, _P, _P, _P, _P, _P, _Z, _P],
     "moe_layer_bwd": [_CFG, ctypes.POINTER(MoeWeights), _P, _P, ctypes.POINTER(MoeSaved), _P,
                       ctypes.POINTER(MoeGrads), _I, _P, _Z, _P],
     "moe_get_device_error": [ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32), _I],
@@ -111,14 +112,14 @@ def _check(fn: str, code: int) -> None:
 
 
 def config(T: int, d_model: int, d_ff: int, E: int, k: int, capacity_factor: float = 0.0, capacity: int = -1,
-           dtype: int = MOE_BF16) -> MoeConfig:
-    return MoeConfig(T, d_model, d_ff, E, k, capacity_factor, capacity, dtype)
+           dtype: int = MOE_BF16, aux_loss_coeff: float = 0.0) -> MoeConfig:
+    return MoeConfig(T, d_model, d_ff, E, k, capacity_factor, capacity, dtype, aux_loss_coeff)
 
 
-def config_of(shape, T: Optional[int] = None) -> MoeConfig:
+def config_of(shape, T: Optional[int] = None, aux_loss_coeff: float = 0.0) -> MoeConfig:
     """Config for a ``workload.LayerShape``."""
     return config(shape.T if T is None else T, shape.d_model, shape.d_ff, shape.E, shape.k, shape.capacity_factor,
-                  shape.capacity, MOE_BF16 if shape.dtype == "bf16" else MOE_F32)
+                  shape.capacity, MOE_BF16 if shape.dtype == "bf16" else MOE_F32, aux_loss_coeff)
 
 
 def _ptr(t) -> int:
@@ -238,11 +239,19 @@ def moe_unpermute_dx_router_bwd(cfg, x, dx_perm, row_of, dl, W_r, dx, dW_r, accu
         int(accumulate), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
+def moe_aux_loss(cfg, probs, ids, loss, dl, ws, stream=None) -> None:
+    """Auxiliary load-balancing loss: writes it to ``loss`` (1 fp32, or None) and adds its
+    logit gradient to ``dl`` [T, E] in place (cfg.aux_loss_coeff; nothing when 0)."""
+    _check("moe_aux_loss", lib().moe_aux_loss(ctypes.byref(cfg), _ptr(probs), _ptr(ids), _ptr(loss), _ptr(dl),
+                                              _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
 def moe_layer_bwd(cfg, weights: dict, x, dy, saved: dict, dx, grads: dict, accumulate: int, ws,
                   stream=None) -> None:
     w = _weights(weights)
     sv = _saved(saved)
-    g = MoeGrads(_ptr(grads["dW_r"]), _ptr(grads["dW1"]), _ptr(grads["dW3"]), _ptr(grads["dW2"]))
+    g = MoeGrads(_ptr(grads["dW_r"]), _ptr(grads["dW1"]), _ptr(grads["dW3"]), _ptr(grads["dW2"]),
+                 _ptr(grads.get("aux_loss")))
     _check("moe_layer_bwd", lib().moe_layer_bwd(
         ctypes.byref(cfg), ctypes.byref(w), _ptr(x), _ptr(dy), ctypes.byref(sv), _ptr(dx), ctypes.byref(g),
         int(accumulate), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
@@ -320,7 +329,7 @@ def allocate_grads(cfg: MoeConfig, device="cuda") -> dict:
     E, d, f = cfg.E, cfg.d_model, cfg.d_ff
     z = dict(dtype=torch.float32, device=device)
     return dict(dW_r=torch.zeros(d, E, **z), dW1=torch.zeros(E, d, f, **z), dW3=torch.zeros(E, d, f, **z),
-                dW2=torch.zeros(E, f, d, **z))
+                dW2=torch.zeros(E, f, d, **z), aux_loss=torch.zeros(1, **z))
 
 
 def workspace(cfg: MoeConfig, training: int, device="cuda"):

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_gb300.so")
-SOURCES = ["moe_api.cu", "routing.cu", "rows.cu", "gemm_simt.cu", "gemm_tc.cu", "noalloc.cu", "router_tc.cu", "selftest.cu", "dwr_tc.cu"]
+SOURCES = ["moe_api.cu", "routing.cu", "rows.cu", "gemm_simt.cu", "gemm_tc.cu", "noalloc.cu", "router_tc.cu", "selftest.cu", "dwr_tc.cu", "aux_loss.cu"]
 HEADERS = ["internal.h", "common.cuh", "tc_ptx.cuh", os.path.join("..", "..", "include", "moe.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -28,6 +28,8 @@ enum KernelKind : int {
   KK_SPLIT_WR,
   KK_SELFTEST,
   KK_SPLIT_DL,
+  KK_AUX_LOSS,
+  KK_AUX_GRAD,
   KK_COUNT
 };
 
@@ -59,6 +61,7 @@ struct Shape {
   int cap;           // INT32_MAX when dropless
   int bf16;          // 1 = bf16 activations/weights, 0 = fp32
   int64_t max_rows;  // bound on offsets[E]
+  float aux;         // auxiliary load-balancing loss coefficient (0: off)
 };
 
 // ---- routing.cu ----
@@ -96,6 +99,11 @@ int dwr_splits(const Shape& s);  // token slices of the router-weight gradient (
 // Adds the token-slice partials [splits][d][E] in slice order into dW_r (n = d * E).
 cudaError_t launch_dwr_reduce(const float* partial, float* dW_r, int splits, int64_t n, int accumulate,
                               cudaStream_t st);
+
+// ---- aux_loss.cu: auxiliary load-balancing loss (adds its logit gradient into dl) ----
+size_t aux_scratch_bytes(const Shape& s);
+cudaError_t launch_aux_loss(const Shape& s, float coeff, const float* probs, const int32_t* ids, float* loss,
+                            float* dl, void* scratch, uint32_t* err, cudaStream_t st);
 
 // ---- dwr_tc.cu: the router-weight gradient on the tensor cores (bf16 layers) ----
 bool dwr_tc_supported(const Shape& s);

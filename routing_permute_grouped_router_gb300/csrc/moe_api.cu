@@ -78,7 +78,7 @@ const char* const kKernelNames[KK_COUNT] = {
     "router_topk",  "slot_scan",  "slot_assign",     "permute",      "gemm_up_swiglu", "gemm_down",
     "unpermute_combine", "combine_bwd", "gemm_dgrad_h_swiglu_bwd", "gemm_wgrad", "gemm_dgrad_x",
     "transpose_wr", "dx_router",  "dwr",     "dwr_reduce",   "zero", "split_wr", "selftest_bounded_wait",
-    "split_dl"};
+    "split_dl", "aux_loss", "aux_grad"};
 
 }  // namespace
 
@@ -136,6 +136,7 @@ moe_status make_shape(const moe_config* c, Shape* s) {
   }
   rows = (rows + 127) / 128 * 128;
   if (rows > (int64_t)INT_MAX - 128) return MOE_ERR_SHAPE;
+  if (!std::isfinite(c->aux_loss_coeff) || c->aux_loss_coeff < 0.f) return MOE_ERR_INVALID_ARG;
   s->T = c->T;
   s->d = c->d_model;
   s->f = c->d_ff;
@@ -144,6 +145,7 @@ moe_status make_shape(const moe_config* c, Shape* s) {
   s->cap = (int)cap;
   s->bf16 = bf16 ? 1 : 0;
   s->max_rows = rows;
+  s->aux = c->aux_loss_coeff;
   return MOE_OK;
 }
 
@@ -190,6 +192,7 @@ struct BwdScratch {
   void *dy_perm, *da, *db, *dx_perm;
   float *dg, *dl, *W_rT, *partial;
   void* dlsplit;  // bf16 parts of dl for the tensor-core router-weight gradient
+  void* aux;      // auxiliary-loss partial sums
 };
 
 RoutingScratch carve_routing(Carver& c, const Shape& s) {
@@ -230,6 +233,7 @@ BwdScratch carve_bwd(Carver& c, const Shape& s) {
   const bool tc = dwr_tc_supported(s);
   b.partial = static_cast<float*>(c.take((size_t)(tc ? dwr_tc_ranges(s) : dwr_splits(s)) * s.d * s.E * 4));
   b.dlsplit = c.take(tc ? dwr_tc_split_bytes(s) : 0);
+  b.aux = c.take(aux_scratch_bytes(s));
   return b;
 }
 size_t ws_bytes_for(const Shape& s, int training) {
@@ -529,6 +533,24 @@ moe_status moe_grouped_ffn_bwd(const moe_config* cfg, const void* x_perm, const 
   return do_ffn_bwd(s, fb, err, stream);
 }
 
+moe_status moe_aux_loss(const moe_config* cfg, const float* probs, const int32_t* ids, float* loss, float* dl,
+                        void* ws, size_t ws_bytes, moe_stream_t stream) {
+  Shape s;
+  MOE_TRY(make_shape(cfg, &s));
+  MOE_TRY(need(probs, 4));
+  MOE_TRY(need(ids, 4));
+  MOE_TRY(need(dl, 4));
+  if (loss != nullptr) MOE_TRY(need(loss, 4));
+  if (ws == nullptr || ws_bytes < ws_bytes_for(s, 1)) return MOE_ERR_WORKSPACE;
+  uint32_t* err = nullptr;
+  MOE_TRY(device_ready(&err));
+  Carver c(align_ws(ws));
+  carve_routing(c, s);
+  BwdScratch bs = carve_bwd(c, s);
+  CUDA_TRY(launch_aux_loss(s, s.aux, probs, ids, loss, dl, bs.aux, err, stream));
+  return MOE_OK;
+}
+
 moe_status moe_unpermute_dx_router_bwd(const moe_config* cfg, const void* x, const void* dx_perm,
                                        const int32_t* row_of, const float* dl, const float* W_r, void* dx,
                                        float* dW_r, int accumulate, void* ws, size_t ws_bytes, moe_stream_t stream) {
@@ -569,7 +591,8 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* w, const void
   for (const void* p : sp) MOE_TRY(need(p));
   const void* sp4[] = {saved->ids, saved->gates, saved->row_of, saved->counts, saved->offsets};
   for (const void* p : sp4) MOE_TRY(need(p, 4));
-  if (s.k == 1) MOE_TRY(need(saved->probs, 4));
+  if (s.k == 1 || s.aux > 0.f) MOE_TRY(need(saved->probs, 4));
+  if (grads->aux_loss != nullptr) MOE_TRY(need(grads->aux_loss, 4));
   MOE_TRY(need(grads->dW_r, 4));
   MOE_TRY(need(grads->dW1));
   MOE_TRY(need(grads->dW3));
@@ -583,6 +606,7 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* w, const void
   if (s.T > 0)
     CUDA_TRY(launch_combine_bwd(s, dy, saved->y_perm, saved->ids, saved->row_of, saved->gates, saved->probs,
                                 saved->counts, saved->offsets, bs.dy_perm, bs.dg, bs.dl, err, stream));
+  CUDA_TRY(launch_aux_loss(s, s.aux, saved->probs, saved->ids, grads->aux_loss, bs.dl, bs.aux, err, stream));
   FfnBwdArgs fb{saved->x_perm, saved->a, saved->b, saved->h, bs.dy_perm, saved->counts, saved->offsets,
                 w->W1, w->W3, w->W2, bs.da, bs.db, bs.dx_perm, grads->dW1, grads->dW3, grads->dW2, accumulate};
   MOE_TRY(do_ffn_bwd(s, fb, err, stream));

@@ -43,11 +43,12 @@ class MoELayer:
         return self.dx
 
 
-def from_workload(wl, device="cuda", training: bool = True, T: Optional[int] = None) -> MoELayer:
+def from_workload(wl, device="cuda", training: bool = True, T: Optional[int] = None,
+                  aux_loss_coeff: float = 0.0) -> MoELayer:
     """Upload a ``workload.Workload``'s weights and build the layer."""
     from . import config_of
 
-    cfg = config_of(wl.shape, T)
+    cfg = config_of(wl.shape, T, aux_loss_coeff)
     bias = None if wl.bias is None else torch.from_numpy(wl.bias).to(device)
     return MoELayer(cfg, torch.from_numpy(wl.W_r).to(device), bias, wl.W1.torch(device), wl.W3.torch(device),
                     wl.W2.torch(device), training=training)

@@ -87,9 +87,11 @@ def test_workspace_sizes_positive(lib):
     (dict(T=-1), "MOE_ERR_SHAPE"), (dict(E=0), "MOE_ERR_SHAPE"), (dict(k=0), "MOE_ERR_SHAPE"),
     (dict(k=9, E=16), "MOE_ERR_SHAPE"), (dict(k=5, E=4), "MOE_ERR_SHAPE"), (dict(E=129), "MOE_ERR_SHAPE"),
     (dict(d_model=100), "MOE_ERR_SHAPE"), (dict(d_ff=320), "MOE_ERR_SHAPE"), (dict(dtype=7), "MOE_ERR_DTYPE"),
+    (dict(aux_loss_coeff=-0.01), "MOE_ERR_INVALID_ARG"), (dict(aux_loss_coeff=float("nan")), "MOE_ERR_INVALID_ARG"),
 ])
 def test_invalid_configs_rejected_on_host(lib, kw, err):
-    base = dict(T=64, d_model=256, d_ff=256, E=4, k=2, capacity_factor=1.0, capacity=-1, dtype=pkg.MOE_BF16)
+    base = dict(T=64, d_model=256, d_ff=256, E=4, k=2, capacity_factor=1.0, capacity=-1, dtype=pkg.MOE_BF16,
+                aux_loss_coeff=0.0)
     base.update(kw)
     cfg = pkg.MoeConfig(*[base[n] for n, _ in pkg.MoeConfig._fields_])
     with pytest.raises(pkg.MoeError) as ei:
