@@ -374,6 +374,21 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     fwd_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(fs, fe)), world)
 
+    # inference forward (no saved state: on bf16 layers the up product gathers
+    # its rows from x, no permuted copy), same protocol
+    Li = layer.from_workload(wl, str(dev), training=False)
+    for _ in range(args.warmup):
+        Li.forward(x)
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        flush.zero_()
+        fs[i].record(stream)
+        Li.forward(x)
+        fe[i].record(stream)
+    torch.cuda.synchronize(dev)
+    inf_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(fs, fe)), world)
+    del Li
+
     # end to end through host buffers: pinned x, dy in; y, dx out
     e2e = None
     if not args.no_e2e:
@@ -486,6 +501,7 @@ def run_ours(args, world, rank, local):
                    "parallelism": f"replicas x{world}",
                    "sms": torch.cuda.get_device_properties(dev).multi_processor_count},
         "fwd_tokens_per_s": world * s.T * args.steps / (fwd_ms / 1e3),
+        "fwd_inference_tokens_per_s": world * s.T * args.steps / (inf_ms / 1e3),
         "grouped_gemm_frac_bf16_peak": round(gemm_flops / (gemm_ms / 1e3) / 1e12 / tflops, 4) if gemm_ms else None,
         "permute_gbs": kernels.get("permute", {}).get("gbs"),
         "roofline": roof,

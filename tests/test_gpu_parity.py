@@ -308,3 +308,21 @@ def test_permute_then_unpermute_is_identity_on_gpu(k):
     check_no_device_error()
     assert (sv["slot"] >= 0).all()
     assert torch.equal(y, x)
+
+
+@pytest.mark.parametrize("shape", [SMALL["top2_e8_small"], SMALL["zipf_e64_small"], SMALL["dropless_e32_small"],
+                                   SMALL["train_f32_small"],
+                                   LS("inf_ragged", 65, 256, 512, 3, 2, 2.0, W.BF16),
+                                   LS("inf_one", 1, 256, 256, 8, 2, 1.25, W.BF16),
+                                   LS("inf_cap0", 200, 256, 256, 4, 2, 1.0, W.BF16, capacity=0),
+                                   LS("inf_e128_k8", 300, 256, 256, 128, 8, 1.0, W.BF16)])
+def test_inference_forward(shape):
+    """Forward without saved state: on bf16 layers the up product gathers its rows
+    from x through src_token (no permuted copy); y must match the oracle."""
+    wl = W.make(shape, seed=12, micro_batches=1, with_dy=False)
+    L = layer.from_workload(wl, training=False)
+    y = L.forward(wl.x[0].torch("cuda"))
+    torch.cuda.synchronize()
+    check_no_device_error()
+    st = _oracle_fwd(wl)
+    assert_close("y", y[: shape.T], st["y"], 1e-4 if shape.dtype == W.F32 else 2e-2)
