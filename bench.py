@@ -49,6 +49,8 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--aux-loss-coeff", type=float, default=0.0,
                    help="auxiliary load-balancing loss coefficient (the layer configurations use none)")
+    p.add_argument("--recompute", action="store_true",
+                   help="keep no a, b, h between forward and backward (the backward recomputes them)")
     return p.parse_args()
 
 
@@ -308,7 +310,7 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     s = W.WORKLOADS[args.workload]
     wl = W.make(s, seed=rank, micro_batches=1, with_dy=True)
-    L = layer.from_workload(wl, str(dev), aux_loss_coeff=args.aux_loss_coeff)
+    L = layer.from_workload(wl, str(dev), aux_loss_coeff=args.aux_loss_coeff, recompute=args.recompute)
     x = wl.x[0].torch(dev)
     dy = wl.dy[0].torch(dev)
     stream = torch.cuda.current_stream(dev)
@@ -495,6 +497,7 @@ def run_ours(args, world, rank, local):
         "vs_baseline": None, "dtype": s.dtype, "data": "synthetic",
         "config": {"workload": args.workload, "T": s.T, "d_model": s.d_model, "d_ff": s.d_ff, "E": s.E, "k": s.k,
                    "capacity_factor": s.capacity_factor, "aux_loss_coeff": args.aux_loss_coeff,
+                   "recompute": args.recompute,
                    "kept_assignments": N,
                    "step": "forward + backward (fp32 grad accumulate)",
                    "l2": "256 MB buffer written before every timed step, outside the step's events",

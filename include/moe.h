@@ -109,7 +109,10 @@ typedef struct {
  * Keeping the assignment indices and the permutation map lets the backward
  * reuse the routing instead of recomputing it ("Recomputation re-runs the
  * dispatch unless you save the permutation", gpu_expert_parallel page).
- * Sizes are in the shape table above. */
+ * Sizes are in the shape table above.  Recompute variant: with a, b and h all
+ * NULL the forward keeps only the routing state, x_perm and y_perm, and the
+ * backward recomputes a, b and h with the same up product (bit for bit the
+ * forward's); the workspace is then moe_workspace_size(cfg, 2) for both calls. */
 typedef struct {
   int32_t* ids;
   float* gates;
@@ -151,7 +154,7 @@ moe_status moe_capacity(const moe_config* cfg, int32_t* C);
 moe_status moe_max_rows(const moe_config* cfg, int64_t* rows);
 
 /* Bytes of workspace that moe_layer_fwd (training = 0) or moe_layer_fwd and
- * moe_layer_bwd (training = 1) need.  The workspace holds the routing
+ * moe_layer_bwd (training = 1; 2 with a, b, h recomputed, see moe_saved) need.  The workspace holds the routing
  * histograms, the forward intermediates when no moe_saved is given, and the
  * backward scratch.  Host only; for bf16 layers the router-weight gradient's
  * partial sums scale with the SM count of the current device, so ask with the

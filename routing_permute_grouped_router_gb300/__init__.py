@@ -305,8 +305,9 @@ def _act_dtype(cfg):
     return torch.bfloat16 if cfg.dtype == MOE_BF16 else torch.float32
 
 
-def allocate_saved(cfg: MoeConfig, device="cuda") -> dict:
-    """Caller-owned routing state and activations for ``moe_layer_fwd``/``moe_layer_bwd``."""
+def allocate_saved(cfg: MoeConfig, device="cuda", recompute: bool = False) -> dict:
+    """Caller-owned routing state and activations for ``moe_layer_fwd``/``moe_layer_bwd``.
+    recompute: keep neither a, b nor h (the backward recomputes them; workspace(cfg, 2))."""
     import torch
 
     R, T, k, E, d, f = moe_max_rows(cfg), max(cfg.T, 1), cfg.k, cfg.E, cfg.d_model, cfg.d_ff
@@ -320,6 +321,13 @@ def allocate_saved(cfg: MoeConfig, device="cuda") -> dict:
                 a=torch.empty(max(R, 1), f, dtype=act, device=device),
                 b=torch.empty(max(R, 1), f, dtype=act, device=device),
                 h=torch.empty(max(R, 1), f, dtype=act, device=device),
+                y_perm=torch.empty(max(R, 1), d, dtype=act, device=device)) if not recompute else dict(
+                ids=torch.empty(T, k, dtype=i32, device=device), gates=torch.empty(T, k, dtype=f32, device=device),
+                slot=torch.empty(T, k, dtype=i32, device=device), row_of=torch.empty(T, k, dtype=i32, device=device),
+                src_token=torch.empty(max(R, 1), dtype=i32, device=device),
+                counts=torch.empty(E, dtype=i32, device=device), offsets=torch.empty(E + 1, dtype=i32, device=device),
+                probs=torch.empty(T, E, dtype=f32, device=device),
+                x_perm=torch.empty(max(R, 1), d, dtype=act, device=device), a=None, b=None, h=None,
                 y_perm=torch.empty(max(R, 1), d, dtype=act, device=device))
 
 

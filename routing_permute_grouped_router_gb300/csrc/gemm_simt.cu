@@ -221,7 +221,7 @@ cudaError_t simt_ffn_fwd(const Shape& s, const FfnFwdArgs& f, uint32_t* err, cud
   a.o1 = static_cast<float*>(f.a);
   a.o2 = static_cast<float*>(f.b);
   cudaError_t e = launch_simt<S_UP>(a, dim3(mt, (s.f + 63) / 64), KK_GEMM_UP, st);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || f.y_perm == nullptr) return e;  // null: the up product alone
   a.h_in = static_cast<const float*>(f.h);
   a.o0 = static_cast<float*>(f.y_perm);
   a.o1 = a.o2 = nullptr;

@@ -856,15 +856,16 @@ cudaError_t tc_ffn_fwd(const Shape& s, const FfnFwdArgs& f, uint32_t* err, cudaS
             make_map(&up.m[2], f.W3, E * d, ff, 64, 64) && make_map(&up.m[3], f.h, R, ff, 64, 32);
   if (f.a != nullptr) ok = ok && make_map(&up.m[4], f.a, R, ff, 64, 32);
   if (f.b != nullptr) ok = ok && make_map(&up.m[5], f.b, R, ff, 64, 32);
-  ok = ok && make_map(&down.m[0], f.h, R, ff, 64, BM) && make_map(&down.m[1], f.W2, E * ff, d, 64, 64) &&
-       make_map(&down.m[2], f.y_perm, R, d, 64, 32);
+  if (f.y_perm != nullptr)  // null: the up product alone (the backward's recompute)
+    ok = ok && make_map(&down.m[0], f.h, R, ff, 64, BM) && make_map(&down.m[1], f.W2, E * ff, d, 64, 64) &&
+         make_map(&down.m[2], f.y_perm, R, d, 64, 32);
   if (!ok) return cudaErrorInvalidValue;
   const int64_t mp = (s.max_rows / BM + s.E + 1) / 2;  // bound on pair tiles of 2 x 128 rows
   a.o0 = static_cast<__nv_bfloat16*>(f.h);
   a.o1 = static_cast<__nv_bfloat16*>(f.a);
   a.o2 = static_cast<__nv_bfloat16*>(f.b);
   cudaError_t e = launch_mode<M_UP>(up, a, mp * (s.f / 128), KK_GEMM_UP, st);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || f.y_perm == nullptr) return e;
   a.o0 = static_cast<__nv_bfloat16*>(f.y_perm);
   a.o1 = a.o2 = nullptr;
   return launch_mode<M_DOWN>(down, a, mp * (s.d / BN), KK_GEMM_DOWN, st);

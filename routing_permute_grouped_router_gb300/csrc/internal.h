@@ -118,7 +118,7 @@ cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t st);
 struct FfnFwdArgs {
   const void* x_perm; const int32_t* counts; const int32_t* offsets;
   const void* W1; const void* W3; const void* W2;
-  void* h; void* y_perm; void* a; void* b;
+  void* h; void* y_perm; void* a; void* b;  // y_perm null: the up product only
 };
 struct FfnBwdArgs {
   const void* x_perm; const void* a; const void* b; const void* h; const void* dy_perm;

@@ -150,6 +150,8 @@ moe_status make_shape(const moe_config* c, Shape* s) {
 }
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+// The recompute variant: the caller keeps none of a, b, h (all three null).
+inline bool recompute_mode(const moe_saved* sv) { return sv->a == nullptr && sv->b == nullptr && sv->h == nullptr; }
 inline moe_status need(const void* p, size_t a = 16) {
   if (p == nullptr) return MOE_ERR_INVALID_ARG;
   return aligned(p, a) ? MOE_OK : MOE_ERR_ALIGNMENT;
@@ -236,11 +238,27 @@ BwdScratch carve_bwd(Carver& c, const Shape& s) {
   b.aux = c.take(aux_scratch_bytes(s));
   return b;
 }
+// a, b, h of the expert FFN when the forward does not keep them (the
+// recompute variant): the forward writes h here for the down product, the
+// backward recomputes all three here before the dgrad.
+struct RecomputeScratch {
+  void *a, *b, *h;
+};
+RecomputeScratch carve_recompute(Carver& c, const Shape& s) {
+  const size_t n = (size_t)s.max_rows * s.f * (s.bf16 ? 2 : 4);
+  RecomputeScratch r;
+  r.a = c.take(n);
+  r.b = c.take(n);
+  r.h = c.take(n);
+  return r;
+}
+// training: 0 inference, 1 training, 2 training with the activations recomputed
 size_t ws_bytes_for(const Shape& s, int training) {
   Carver c(nullptr);
   carve_routing(c, s);
   if (training) carve_bwd(c, s);
   else carve_fwd(c, s);
+  if (training == 2) carve_recompute(c, s);
   return c.off + ALIGN;  // room to align an unaligned base
 }
 void* align_ws(void* ws) {
@@ -347,7 +365,7 @@ moe_status moe_max_rows(const moe_config* cfg, int64_t* rows) {
 moe_status moe_workspace_size(const moe_config* cfg, int training, size_t* bytes) {
   Shape s;
   MOE_TRY(make_shape(cfg, &s));
-  if (bytes == nullptr || (training != 0 && training != 1)) return MOE_ERR_INVALID_ARG;
+  if (bytes == nullptr || training < 0 || training > 2) return MOE_ERR_INVALID_ARG;
   *bytes = ws_bytes_for(s, training);
   return MOE_OK;
 }
@@ -449,14 +467,17 @@ moe_status moe_layer_fwd(const moe_config* cfg, const moe_weights* w, const void
     MOE_TRY(need(saved->offsets, 4));
     MOE_TRY(need(saved->probs, 4));
     MOE_TRY(need(saved->x_perm));
-    MOE_TRY(need(saved->a));
-    MOE_TRY(need(saved->b));
-    MOE_TRY(need(saved->h));
     MOE_TRY(need(saved->y_perm));
+    if (!recompute_mode(saved)) {
+      MOE_TRY(need(saved->a));
+      MOE_TRY(need(saved->b));
+      MOE_TRY(need(saved->h));
+    }
   }
   Carver probe(nullptr);
   carve_routing(probe, s);
-  const size_t need_ws = saved != nullptr ? probe.off + ALIGN : ws_bytes_for(s, 0);
+  const size_t need_ws = saved == nullptr ? ws_bytes_for(s, 0)
+                         : recompute_mode(saved) ? ws_bytes_for(s, 2) : probe.off + ALIGN;
   if (ws == nullptr || ws_bytes < need_ws) return MOE_ERR_WORKSPACE;
   uint32_t* err = nullptr;
   MOE_TRY(device_ready(&err));
@@ -479,6 +500,10 @@ moe_status moe_layer_fwd(const moe_config* cfg, const moe_weights* w, const void
     a = saved->a;
     b = saved->b;
     probs = saved->probs;
+    if (recompute_mode(saved)) {  // h lives in the workspace; a and b are not kept
+      carve_bwd(c, s);
+      f.h = carve_recompute(c, s).h;
+    }
   } else {
     f = carve_fwd(c, s);
   }
@@ -587,8 +612,14 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* w, const void
   MOE_TRY(need(w->W1));
   MOE_TRY(need(w->W3));
   MOE_TRY(need(w->W2));
-  const void* sp[] = {saved->x_perm, saved->a, saved->b, saved->h, saved->y_perm};
-  for (const void* p : sp) MOE_TRY(need(p));
+  const bool recompute = recompute_mode(saved);
+  MOE_TRY(need(saved->x_perm));
+  MOE_TRY(need(saved->y_perm));
+  if (!recompute) {
+    MOE_TRY(need(saved->a));
+    MOE_TRY(need(saved->b));
+    MOE_TRY(need(saved->h));
+  }
   const void* sp4[] = {saved->ids, saved->gates, saved->row_of, saved->counts, saved->offsets};
   for (const void* p : sp4) MOE_TRY(need(p, 4));
   if (s.k == 1 || s.aux > 0.f) MOE_TRY(need(saved->probs, 4));
@@ -597,17 +628,28 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* w, const void
   MOE_TRY(need(grads->dW1));
   MOE_TRY(need(grads->dW3));
   MOE_TRY(need(grads->dW2));
-  if (ws == nullptr || ws_bytes < ws_bytes_for(s, 1)) return MOE_ERR_WORKSPACE;
+  if (ws == nullptr || ws_bytes < ws_bytes_for(s, recompute ? 2 : 1)) return MOE_ERR_WORKSPACE;
   uint32_t* err = nullptr;
   MOE_TRY(device_ready(&err));
   Carver c(align_ws(ws));
   carve_routing(c, s);
   BwdScratch bs = carve_bwd(c, s);
+  const void *act_a = saved->a, *act_b = saved->b, *act_h = saved->h;
+  if (recompute && s.T > 0) {
+    // the up product again from the kept x_perm: a, b and h, bit for bit the
+    // forward's (same kernel, same inputs); no down product
+    const RecomputeScratch rc = carve_recompute(c, s);
+    FfnFwdArgs up{saved->x_perm, saved->counts, saved->offsets, w->W1, w->W3, w->W2, rc.h, nullptr, rc.a, rc.b};
+    MOE_TRY(do_ffn_fwd(s, up, err, stream));
+    act_a = rc.a;
+    act_b = rc.b;
+    act_h = rc.h;
+  }
   if (s.T > 0)
     CUDA_TRY(launch_combine_bwd(s, dy, saved->y_perm, saved->ids, saved->row_of, saved->gates, saved->probs,
                                 saved->counts, saved->offsets, bs.dy_perm, bs.dg, bs.dl, err, stream));
   CUDA_TRY(launch_aux_loss(s, s.aux, saved->probs, saved->ids, grads->aux_loss, bs.dl, bs.aux, err, stream));
-  FfnBwdArgs fb{saved->x_perm, saved->a, saved->b, saved->h, bs.dy_perm, saved->counts, saved->offsets,
+  FfnBwdArgs fb{saved->x_perm, act_a, act_b, act_h, bs.dy_perm, saved->counts, saved->offsets,
                 w->W1, w->W3, w->W2, bs.da, bs.db, bs.dx_perm, grads->dW1, grads->dW3, grads->dW2, accumulate};
   MOE_TRY(do_ffn_bwd(s, fb, err, stream));
   return do_dx_router(s, x, bs.dx_perm, saved->row_of, bs.dl, w->W_r, dx, grads->dW_r, accumulate, bs, err, stream);

@@ -16,7 +16,7 @@ from . import (MOE_BF16, MoeConfig, allocate_grads, allocate_saved, moe_layer_bw
 
 class MoELayer:
     def __init__(self, cfg: MoeConfig, W_r: torch.Tensor, bias: Optional[torch.Tensor], W1: torch.Tensor,
-                 W3: torch.Tensor, W2: torch.Tensor, training: bool = True):
+                 W3: torch.Tensor, W2: torch.Tensor, training: bool = True, recompute: bool = False):
         self.cfg = cfg
         self.device = W1.device
         self.act_dtype = torch.bfloat16 if cfg.dtype == MOE_BF16 else torch.float32
@@ -24,9 +24,10 @@ class MoELayer:
                             W1=W1.contiguous(), W3=W3.contiguous(), W2=W2.contiguous())
         self.training = training
         self.max_rows = moe_max_rows(cfg)
-        self.saved = allocate_saved(cfg, self.device) if training else None
+        self.recompute = training and recompute  # keep no a, b, h: the backward recomputes them
+        self.saved = allocate_saved(cfg, self.device, self.recompute) if training else None
         self.grads = allocate_grads(cfg, self.device) if training else None
-        self.ws = workspace(cfg, 1 if training else 0, self.device)
+        self.ws = workspace(cfg, (2 if self.recompute else 1) if training else 0, self.device)
         T, d = max(cfg.T, 1), cfg.d_model
         self.y = torch.empty(T, d, dtype=self.act_dtype, device=self.device)
         self.dx = torch.empty(T, d, dtype=self.act_dtype, device=self.device) if training else None
@@ -44,11 +45,11 @@ class MoELayer:
 
 
 def from_workload(wl, device="cuda", training: bool = True, T: Optional[int] = None,
-                  aux_loss_coeff: float = 0.0) -> MoELayer:
+                  aux_loss_coeff: float = 0.0, recompute: bool = False) -> MoELayer:
     """Upload a ``workload.Workload``'s weights and build the layer."""
     from . import config_of
 
     cfg = config_of(wl.shape, T, aux_loss_coeff)
     bias = None if wl.bias is None else torch.from_numpy(wl.bias).to(device)
     return MoELayer(cfg, torch.from_numpy(wl.W_r).to(device), bias, wl.W1.torch(device), wl.W3.torch(device),
-                    wl.W2.torch(device), training=training)
+                    wl.W2.torch(device), training=training, recompute=recompute)

@@ -118,3 +118,12 @@ def test_kernel_names(lib):
     names = [lib.moe_kernel_name(i).decode() for i in range(n)]
     assert "gemm_up_swiglu" in names and "permute" in names and len(set(names)) == n
     assert lib.moe_kernel_name(n) is None
+
+
+def test_recompute_workspace_is_larger_and_training_flag_checked(lib):
+    cfg = pkg.config(1000, 256, 512, 8, 2, 1.25)
+    w1, w2 = pkg.moe_workspace_size(cfg, 1), pkg.moe_workspace_size(cfg, 2)
+    R = pkg.moe_max_rows(cfg)
+    assert w2 - w1 >= 3 * R * 512 * 2  # a, b, h of the recompute
+    with pytest.raises(pkg.MoeError):
+        pkg.moe_workspace_size(cfg, 3)

@@ -326,3 +326,28 @@ def test_inference_forward(shape):
     check_no_device_error()
     st = _oracle_fwd(wl)
     assert_close("y", y[: shape.T], st["y"], 1e-4 if shape.dtype == W.F32 else 2e-2)
+
+
+@pytest.mark.parametrize("name", ["train_e16_small", "top2_e8_small", "train_f32_small"])
+def test_recompute_variant_is_bitwise_the_saving_path(name):
+    """Keeping neither a, b nor h (the backward recomputes them with the same up
+    product) gives y, dx and every gradient bit for bit as the layer that keeps
+    them, over two accumulated micro-batches."""
+    s = SMALL[name]
+    wl = W.make(s, seed=21, micro_batches=2, with_dy=True)
+    res = []
+    for recompute in (False, True):
+        L = layer.from_workload(wl, recompute=recompute)
+        assert (L.saved["a"] is None) == recompute
+        out = []
+        for m in range(2):
+            x, dy = wl.x[m].torch("cuda"), wl.dy[m].torch("cuda")
+            L.forward(x)
+            L.backward(x, dy, accumulate=m > 0)
+            torch.cuda.synchronize()
+            check_no_device_error()
+            out += [L.y[: s.T].clone(), L.dx[: s.T].clone()]
+        out += [L.grads[n].clone() for n in ("dW_r", "dW1", "dW3", "dW2")]
+        res.append(out)
+    for u, v in zip(*res):
+        assert torch.equal(u, v)
