@@ -1,8 +1,10 @@
 // Inline-PTX wrappers for sm_103a tensor-core kernels: mbarriers with bounded
-// waits, TMA loads/stores/reductions, tcgen05 (TMEM allocation, MMA, commit,
-// TMEM loads) and the shared-memory matrix descriptor of the 128-byte swizzle.
-// Shared by the grouped GEMM (gemm_tc.cu) and the tensor-core router
-// (router_tc.cu); both live in an anonymous namespace per translation unit.
+// waits, TMA loads and stores, tcgen05 (TMEM allocation, MMA, commit, TMEM
+// loads; single-CTA and CTA-pair forms), cluster helpers and the
+// shared-memory matrix descriptor of the 128-byte swizzle.
+// Shared by the grouped GEMM (gemm_tc.cu), the tensor-core router
+// (router_tc.cu) and the router-weight gradient (dwr_tc.cu); each gets its
+// own copy in an anonymous namespace per translation unit.
 #pragma once
 
 #include <cuda.h>
@@ -120,15 +122,9 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
 }
 __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) { asm volatile("" : TMEM_REGS32(r)::"memory"); }
 
-// TMA stores / reductions from shared memory, tracked with bulk groups.
+// TMA stores from shared memory, tracked with bulk groups.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(src), "r"(c0), "r"(c1)
-               : "memory");
-}
-__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
-  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
                "r"(src), "r"(c0), "r"(c1)
                : "memory");
