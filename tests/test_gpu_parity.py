@@ -351,3 +351,23 @@ def test_recompute_variant_is_bitwise_the_saving_path(name):
         res.append(out)
     for u, v in zip(*res):
         assert torch.equal(u, v)
+
+
+@pytest.mark.parametrize("E,k", [(8, 2), (32, 4), (64, 2)])
+def test_router_more_tiles_than_sms_matches_oracle(E, k):
+    """More 128-token tiles than SMs (the router runs without a K split, two CTAs
+    an SM up to 32 experts, each tile starting its K loop at its own k-block):
+    routing must match the oracle bit for bit and the probabilities and gates to
+    fp32 rounding."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    T = 128 * (sms + 3) + 44  # an odd tile count, the last tile partial
+    s = LS(f"two_tiles_e{E}", T, 256, 256, E, k, 1.25, W.BF16)
+    wl = W.make(s, seed=14, micro_batches=1, with_dy=False)
+    L = layer.from_workload(wl)
+    L.forward(wl.x[0].torch("cuda"))
+    torch.cuda.synchronize()
+    check_no_device_error()
+    st = O.route(wl.x[0].f64(), wl.W_r, wl.bias, k, _cap(s))
+    assert_routing_equal(L.saved, st, T)
+    assert_close("probs", L.saved["probs"], st["probs"], 1e-5)
+    assert_close("gates", L.saved["gates"], st["gates"], 1e-5)
