@@ -20,8 +20,9 @@
 // CTAs r > 0 park their partial logits in their shared memory; the first CTA
 // adds them over distributed shared memory in rank order (so the sum does not
 // depend on timing) and does softmax and top-k in registers (value
-// descending, lower expert index on ties).  The histogram is written per
-// 64-token block, the layout the slot scan reads.
+// descending, lower expert index on ties), staging the probabilities in its
+// shared memory so the tile's rows leave as one contiguous run.  The
+// histogram is written per 64-token block, the layout the slot scan reads.
 #include <cudaTypedefs.h>
 #include <float.h>
 
@@ -83,6 +84,84 @@ __global__ void split_wr_kernel(const float* W_r, __nv_bfloat16* wsplit, int d, 
   wsplit[i] = hi;
   wsplit[plane + i] = mid;
   wsplit[2 * plane + i] = lo;
+}
+
+// One token's logits v (no bias yet) -> bias, top-k (value descending, lower
+// expert index on ties; taken first, so the maximum is the first pick), fp32
+// softmax (probabilities written to prow unless it is null), gates and ids;
+// the picks are returned in ej for the caller's histogram.
+template <int N>
+__device__ __forceinline__ void token_epilogue(const RouterTcArgs& a, float (&v)[N], int t, float* prow,
+                                               int (&ej)[R_MAXK]) {
+#pragma unroll
+  for (int e = 0; e < N; ++e) {
+    float l = -INFINITY;
+    if (e < a.E) {
+      l = v[e] + (a.bias != nullptr ? __ldg(a.bias + e) : 0.f);
+      if (isnan(l)) l = -INFINITY;
+    }
+    v[e] = l;
+  }
+  // if every untaken logit is -inf the lowest untaken index is picked
+  constexpr int NW = (N + 31) / 32;
+  uint32_t taken[NW];
+#pragma unroll
+  for (int w = 0; w < NW; ++w) taken[w] = 0u;
+  float lj[R_MAXK];
+#pragma unroll
+  for (int j = 0; j < R_MAXK; ++j) {
+    lj[j] = 0.f;
+    ej[j] = 0;
+    if (j < a.k) {
+      float bv = -INFINITY;
+      int be = -1;
+#pragma unroll
+      for (int e = 0; e < N; ++e)
+        if (e < a.E && !((taken[e >> 5] >> (e & 31)) & 1u) && (be < 0 || v[e] > bv)) {  // strict: lower index on ties
+          bv = v[e];
+          be = e;
+        }
+#pragma unroll
+      for (int w = 0; w < NW; ++w)
+        if ((be >> 5) == w) taken[w] |= 1u << (be & 31);
+      lj[j] = bv;
+      ej[j] = be;
+    }
+  }
+  const float mx = lj[0];
+  float se = 0.f;
+#pragma unroll
+  for (int e = 0; e < N; ++e)
+    if (e < a.E) {
+      v[e] = expf(v[e] - mx);
+      se += v[e];
+    }
+  if (prow != nullptr) {
+#pragma unroll
+    for (int e = 0; e < N; ++e)
+      if (e < a.E) prow[e] = v[e] / se;
+  }
+  float g[R_MAXK];
+  if (a.k == 1) {
+    g[0] = expf(lj[0] - mx) / se;
+  } else {
+    float den = 0.f;
+#pragma unroll
+    for (int j = 0; j < R_MAXK; ++j)
+      if (j < a.k) {
+        g[j] = expf(lj[j] - lj[0]);
+        den += g[j];
+      }
+#pragma unroll
+    for (int j = 0; j < R_MAXK; ++j)
+      if (j < a.k) g[j] = g[j] / den;
+  }
+#pragma unroll
+  for (int j = 0; j < R_MAXK; ++j)
+    if (j < a.k) {
+      a.ids[(size_t)t * a.k + j] = ej[j];
+      a.gates[(size_t)t * a.k + j] = g[j];
+    }
 }
 
 template <int N>
@@ -243,93 +322,31 @@ __global__ void __launch_bounds__(R_THREADS, RCfg<N>::MIN_BLOCKS) router_tc_kern
       const uint32_t off = smem_addr(smem) + (uint32_t)row * PSTRIDE * 4;
       for (uint32_t r = 1; r < cs; ++r) {
         const uint32_t src = mapa_shared(off, r);
+        // up to eight loads in flight before their first use
+        constexpr int B = N / 4 < 8 ? N / 4 : 8;
 #pragma unroll
-        for (int c = 0; c < N / 4; ++c) {
-          const float4 p = ld_shared_cluster_f4(src + 16 * c);
-          v[4 * c] += p.x;
-          v[4 * c + 1] += p.y;
-          v[4 * c + 2] += p.z;
-          v[4 * c + 3] += p.w;
+        for (int c0 = 0; c0 < N / 4; c0 += B) {
+          float4 pv[B];
+#pragma unroll
+          for (int c = 0; c < B; ++c) pv[c] = ld_shared_cluster_f4(src + 16 * (c0 + c));
+#pragma unroll
+          for (int c = 0; c < B; ++c) {
+            v[4 * (c0 + c)] += pv[c].x;
+            v[4 * (c0 + c) + 1] += pv[c].y;
+            v[4 * (c0 + c) + 2] += pv[c].z;
+            v[4 * (c0 + c) + 3] += pv[c].w;
+          }
         }
       }
     }
     if (have && t < a.T) {
-      float mx = -INFINITY;
-#pragma unroll
-      for (int e = 0; e < N; ++e) {
-        float l = -INFINITY;
-        if (e < a.E) {
-          l = v[e] + (a.bias != nullptr ? __ldg(a.bias + e) : 0.f);
-          if (isnan(l)) l = -INFINITY;
-        }
-        v[e] = l;
-        mx = fmaxf(mx, l);
-      }
-      float se = 0.f;
-#pragma unroll
-      for (int e = 0; e < N; ++e)
-        if (e < a.E) se += expf(v[e] - mx);
-      if (a.probs != nullptr) {
-        float* pr = a.probs + (size_t)t * a.E;
-#pragma unroll
-        for (int e = 0; e < N; ++e)
-          if (e < a.E) pr[e] = expf(v[e] - mx) / se;
-      }
-      float lj[R_MAXK];
       int ej[R_MAXK];
-#pragma unroll
-      for (int j = 0; j < R_MAXK; ++j) {
-        lj[j] = 0.f;
-        ej[j] = 0;
-        if (j < a.k) {
-          float bv = -INFINITY;
-          int be = -1;
-#pragma unroll
-          for (int e = 0; e < N; ++e)
-            if (e < a.E && (be < 0 || v[e] > bv)) {  // strict: the lower index wins ties
-              bv = v[e];
-              be = e;
-            }
-#pragma unroll
-          for (int e = 0; e < N; ++e)
-            if (e == be) v[e] = -INFINITY;
-          // a taken expert is -inf; if every remaining logit is -inf the
-          // lowest untaken index still has to be found
-          if (bv == -INFINITY) {
-            be = -1;
-            for (int e = 0; e < a.E && be < 0; ++e) {
-              bool used = false;
-              for (int jj = 0; jj < j; ++jj) used |= ej[jj] == e;
-              if (!used) be = e;
-            }
-          }
-          lj[j] = bv;
-          ej[j] = be;
-        }
-      }
-      float g[R_MAXK];
-      if (a.k == 1) {
-        g[0] = expf(lj[0] - mx) / se;
-      } else {
-        float den = 0.f;
-#pragma unroll
-        for (int j = 0; j < R_MAXK; ++j)
-          if (j < a.k) {
-            g[j] = expf(lj[j] - lj[0]);
-            den += g[j];
-          }
-#pragma unroll
-        for (int j = 0; j < R_MAXK; ++j)
-          if (j < a.k) g[j] = g[j] / den;
-      }
-      const int half = row / HIST_TOK;
+      // rank 0's stage buffers are free once its MMAs are done: probabilities go there
+      token_epilogue<N>(a, v, t, a.probs != nullptr ? reinterpret_cast<float*>(smem) + (size_t)row * PSTRIDE : nullptr,
+                        ej);
 #pragma unroll
       for (int j = 0; j < R_MAXK; ++j)
-        if (j < a.k) {
-          a.ids[(size_t)t * a.k + j] = ej[j];
-          a.gates[(size_t)t * a.k + j] = g[j];
-          atomicAdd(&hist_s[half][j][ej[j]], 1);
-        }
+        if (j < a.k) atomicAdd(&hist_s[row / HIST_TOK][j][ej[j]], 1);
     }
   }
   if (cs > 1) cluster_sync();  // the first CTA has read every partial
@@ -337,6 +354,12 @@ __global__ void __launch_bounds__(R_THREADS, RCfg<N>::MIN_BLOCKS) router_tc_kern
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (rank == 0 && a.probs != nullptr) {  // the tile's probabilities are contiguous in [T, E]
+    const int n = min(RT, a.T - tile * RT);
+    const float* stage = reinterpret_cast<const float*>(smem);
+    float* dst = a.probs + (size_t)tile * RT * a.E;
+    for (int i = threadIdx.x; i < n * a.E; i += R_THREADS) dst[i] = stage[(i / a.E) * PSTRIDE + i % a.E];
+  }
   // histogram of the two 64-token blocks of this tile, laid out [e][j][block]
   for (int i = threadIdx.x; i < 2 * a.k * a.E && rank == 0; i += R_THREADS) {
     const int half = i / (a.k * a.E), r = i % (a.k * a.E), j = r / a.E, e = r % a.E;

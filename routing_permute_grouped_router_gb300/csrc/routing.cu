@@ -249,18 +249,37 @@ __global__ void __launch_bounds__(256) slot_scan_kernel(ScanArgs a) {
   __syncthreads();
   if (tid == 0) is_last = (atomicAdd(a.ticket, 1) == (int)gridDim.x - 1);
   __syncthreads();
-  if (is_last && tid == 0) {
+  if (is_last) {
+    // counts[e] = min(total, C) and the 128-aligned offsets: one expert per
+    // thread (E <= 128), an exclusive scan of the padded counts over the block
+    __shared__ int64_t pad_sums[8];
     __threadfence();
-    int64_t off = 0;
-    for (int x = 0; x < a.E; ++x) {
-      const int tot = __ldcg(a.totals + x);
-      const int c = tot < a.cap ? tot : a.cap;
-      a.counts[x] = c;
-      a.offsets[x] = (int32_t)off;
-      off += ((int64_t)c + 127) / 128 * 128;
+    int c = 0;
+    int64_t padded = 0;
+    if (tid < a.E) {
+      const int tot = __ldcg(a.totals + tid);
+      c = tot < a.cap ? tot : a.cap;
+      padded = ((int64_t)c + 127) / 128 * 128;
     }
-    if (off > a.max_rows) report_error(a.err, DEV_BAD_OFFSETS, 1);
-    a.offsets[a.E] = (int32_t)(off > a.max_rows ? a.max_rows : off);
+    int64_t pincl = padded;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t n = __shfl_up_sync(0xffffffffu, pincl, o);
+      if (lane >= o) pincl += n;
+    }
+    if (lane == 31) pad_sums[warp] = pincl;
+    __syncthreads();
+    int64_t off = pincl - padded;
+    for (int w = 0; w < warp; ++w) off += pad_sums[w];
+    if (tid < a.E) {
+      a.counts[tid] = c;
+      a.offsets[tid] = (int32_t)off;
+    }
+    if (tid == a.E - 1) {
+      const int64_t end = off + padded;
+      if (end > a.max_rows) report_error(a.err, DEV_BAD_OFFSETS, 1);
+      a.offsets[a.E] = (int32_t)(end > a.max_rows ? a.max_rows : end);
+    }
   }
 }
 
