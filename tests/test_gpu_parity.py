@@ -353,14 +353,15 @@ def test_recompute_variant_is_bitwise_the_saving_path(name):
         assert torch.equal(u, v)
 
 
-@pytest.mark.parametrize("E,k", [(8, 2), (32, 4), (64, 2)])
-def test_router_more_tiles_than_sms_matches_oracle(E, k):
+@pytest.mark.parametrize("E,k,extra", [(8, 2, 3), (32, 4, 3), (64, 2, 3), (32, 2, 2), (5, 1, 2), (128, 8, 3)])
+def test_router_more_tiles_than_sms_matches_oracle(E, k, extra):
     """More 128-token tiles than SMs (the router runs without a K split, two CTAs
-    an SM up to 32 experts, each tile starting its K loop at its own k-block):
-    routing must match the oracle bit for bit and the probabilities and gates to
-    fp32 rounding."""
+    an SM up to 32 experts, each tile starting its K loop at its own k-block;
+    even and odd tile counts, expert padding with E = 5, and E = 128 with k = 8):
+    routing must match the oracle bit for bit and the probabilities and gates
+    to fp32 rounding."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    T = 128 * (sms + 3) + 44  # an odd tile count, the last tile partial
+    T = 128 * (sms + extra) + 44  # sms + extra + 1 tiles, the last one partial
     s = LS(f"two_tiles_e{E}", T, 256, 256, E, k, 1.25, W.BF16)
     wl = W.make(s, seed=14, micro_batches=1, with_dy=False)
     L = layer.from_workload(wl)
