@@ -129,17 +129,19 @@ __device__ __forceinline__ void token_epilogue(const RouterTcArgs& a, float (&v)
     }
   }
   const float mx = lj[0];
+  // the exponentials first (independent, so they overlap), then their sum in
+  // expert order
+#pragma unroll
+  for (int e = 0; e < N; ++e) v[e] = e < a.E ? expf(v[e] - mx) : 0.f;
   float se = 0.f;
 #pragma unroll
   for (int e = 0; e < N; ++e)
-    if (e < a.E) {
-      v[e] = expf(v[e] - mx);
-      se += v[e];
-    }
+    if (e < a.E) se += v[e];
   if (prow != nullptr) {
+    const float inv = 1.f / se;  // one division; each probability within an ulp of exp / sum
 #pragma unroll
     for (int e = 0; e < N; ++e)
-      if (e < a.E) prow[e] = v[e] / se;
+      if (e < a.E) prow[e] = v[e] * inv;
   }
   float g[R_MAXK];
   if (a.k == 1) {
@@ -354,11 +356,12 @@ __global__ void __launch_bounds__(R_THREADS, RCfg<N>::MIN_BLOCKS) router_tc_kern
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (rank == 0 && a.probs != nullptr) {  // the tile's probabilities are contiguous in [T, E]
+  if (rank == 0 && a.probs != nullptr) {  // the tile's probabilities, a row per warp at a time
     const int n = min(RT, a.T - tile * RT);
     const float* stage = reinterpret_cast<const float*>(smem);
     float* dst = a.probs + (size_t)tile * RT * a.E;
-    for (int i = threadIdx.x; i < n * a.E; i += R_THREADS) dst[i] = stage[(i / a.E) * PSTRIDE + i % a.E];
+    for (int r = warp; r < n; r += R_THREADS / 32)
+      for (int e = lane; e < a.E; e += 32) dst[(size_t)r * a.E + e] = stage[r * PSTRIDE + e];
   }
   // histogram of the two 64-token blocks of this tile, laid out [e][j][block]
   for (int i = threadIdx.x; i < 2 * a.k * a.E && rank == 0; i += R_THREADS) {
