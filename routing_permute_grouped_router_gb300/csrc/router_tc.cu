@@ -20,9 +20,8 @@
 // CTAs r > 0 park their partial logits in their shared memory; the first CTA
 // adds them over distributed shared memory in rank order (so the sum does not
 // depend on timing) and does softmax and top-k in registers (value
-// descending, lower expert index on ties), staging the probabilities in its
-// shared memory so the tile's rows leave as one contiguous run.  The
-// histogram is written per 64-token block, the layout the slot scan reads.
+// descending, lower expert index on ties).  The histogram is written per
+// 64-token block, the layout the slot scan reads.
 #include <cudaTypedefs.h>
 #include <float.h>
 
@@ -86,23 +85,26 @@ __global__ void split_wr_kernel(const float* W_r, __nv_bfloat16* wsplit, int d, 
   wsplit[2 * plane + i] = lo;
 }
 
-// One token's logits v (no bias yet) -> bias, top-k (value descending, lower
-// expert index on ties; taken first, so the maximum is the first pick), fp32
-// softmax (probabilities written to prow unless it is null), gates and ids;
-// the picks are returned in ej for the caller's histogram.
+// One token's logits v (no bias yet) -> bias (bias_s: the bias in shared
+// memory, zero without one), top-k (value descending, lower expert index on
+// ties; taken first, so the maximum is the first pick), fp32 softmax
+// (probabilities written to the token's row prow of [T, E] unless it is null),
+// gates and ids; the picks are returned in ej for the caller's histogram.
 template <int N>
-__device__ __forceinline__ void token_epilogue(const RouterTcArgs& a, float (&v)[N], int t, float* prow,
-                                               int (&ej)[R_MAXK]) {
+__device__ __forceinline__ void token_epilogue(const RouterTcArgs& a, float (&v)[N], int t, const float* bias_s,
+                                               float* prow, int (&ej)[R_MAXK]) {
 #pragma unroll
   for (int e = 0; e < N; ++e) {
     float l = -INFINITY;
     if (e < a.E) {
-      l = v[e] + (a.bias != nullptr ? __ldg(a.bias + e) : 0.f);
+      l = v[e] + bias_s[e];
       if (isnan(l)) l = -INFINITY;
     }
     v[e] = l;
   }
-  // if every untaken logit is -inf the lowest untaken index is picked
+  // if every untaken logit is -inf the lowest untaken index is picked; the
+  // padding experts e >= E hold -inf and come after every real one, so they
+  // never win (k <= E)
   constexpr int NW = (N + 31) / 32;
   uint32_t taken[NW];
 #pragma unroll
@@ -117,7 +119,7 @@ __device__ __forceinline__ void token_epilogue(const RouterTcArgs& a, float (&v)
       int be = -1;
 #pragma unroll
       for (int e = 0; e < N; ++e)
-        if (e < a.E && !((taken[e >> 5] >> (e & 31)) & 1u) && (be < 0 || v[e] > bv)) {  // strict: lower index on ties
+        if (!((taken[e >> 5] >> (e & 31)) & 1u) && (be < 0 || v[e] > bv)) {  // strict: lower index on ties
           bv = v[e];
           be = e;
         }
@@ -139,9 +141,17 @@ __device__ __forceinline__ void token_epilogue(const RouterTcArgs& a, float (&v)
     if (e < a.E) se += v[e];
   if (prow != nullptr) {
     const float inv = 1.f / se;  // one division; each probability within an ulp of exp / sum
+    if ((a.E & 3) == 0) {  // the row starts on 16 bytes: whole float4 pieces
 #pragma unroll
-    for (int e = 0; e < N; ++e)
-      if (e < a.E) prow[e] = v[e] * inv;
+      for (int c = 0; c < N / 4; ++c)
+        if (4 * c < a.E)
+          reinterpret_cast<float4*>(prow)[c] =
+              make_float4(v[4 * c] * inv, v[4 * c + 1] * inv, v[4 * c + 2] * inv, v[4 * c + 3] * inv);
+    } else {
+#pragma unroll
+      for (int e = 0; e < N; ++e)
+        if (e < a.E) prow[e] = v[e] * inv;
+    }
   }
   float g[R_MAXK];
   if (a.k == 1) {
@@ -174,6 +184,7 @@ __global__ void __launch_bounds__(R_THREADS, RCfg<N>::MIN_BLOCKS) router_tc_kern
   constexpr int PSTRIDE = N + 4;  // floats per parked row (16-byte rows, no bank conflicts)
   extern __shared__ uint8_t smem_raw[];
   __shared__ int hist_s[2][R_MAXK][N];
+  __shared__ float bias_s[N];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::CTRL_OFF);
   uint64_t* empty_bar = full_bar + 8;
@@ -197,6 +208,7 @@ __global__ void __launch_bounds__(R_THREADS, RCfg<N>::MIN_BLOCKS) router_tc_kern
   }
   for (int i = threadIdx.x; i < 2 * R_MAXK * N; i += R_THREADS) (&hist_s[0][0][0])[i] = 0;
   pdl_enter();  // no global memory or TMEM access above this line
+  for (int e = threadIdx.x; e < N; e += R_THREADS) bias_s[e] = (a.bias != nullptr && e < a.E) ? a.bias[e] : 0.f;
   if (threadIdx.x == 0 && tile == 0 && rank == 0) *a.ticket = 0;  // for the last-block election of the slot scan
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), C::TCOLS);
@@ -344,8 +356,7 @@ __global__ void __launch_bounds__(R_THREADS, RCfg<N>::MIN_BLOCKS) router_tc_kern
     if (have && t < a.T) {
       int ej[R_MAXK];
       // rank 0's stage buffers are free once its MMAs are done: probabilities go there
-      token_epilogue<N>(a, v, t, a.probs != nullptr ? reinterpret_cast<float*>(smem) + (size_t)row * PSTRIDE : nullptr,
-                        ej);
+      token_epilogue<N>(a, v, t, bias_s, a.probs != nullptr ? a.probs + (size_t)t * a.E : nullptr, ej);
 #pragma unroll
       for (int j = 0; j < R_MAXK; ++j)
         if (j < a.k) atomicAdd(&hist_s[row / HIST_TOK][j][ej[j]], 1);
@@ -356,13 +367,6 @@ __global__ void __launch_bounds__(R_THREADS, RCfg<N>::MIN_BLOCKS) router_tc_kern
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (rank == 0 && a.probs != nullptr) {  // the tile's probabilities, a row per warp at a time
-    const int n = min(RT, a.T - tile * RT);
-    const float* stage = reinterpret_cast<const float*>(smem);
-    float* dst = a.probs + (size_t)tile * RT * a.E;
-    for (int r = warp; r < n; r += R_THREADS / 32)
-      for (int e = lane; e < a.E; e += 32) dst[(size_t)r * a.E + e] = stage[r * PSTRIDE + e];
-  }
   // histogram of the two 64-token blocks of this tile, laid out [e][j][block]
   for (int i = threadIdx.x; i < 2 * a.k * a.E && rank == 0; i += R_THREADS) {
     const int half = i / (a.k * a.E), r = i % (a.k * a.E), j = r / a.E, e = r % a.E;
