@@ -69,3 +69,10 @@ def test_reference_arm_under_torchrun_prints_once():
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["n_gpus"] == 2 and rec["value"] > 0
     assert rec["e2e"]["h2d_bytes_per_step"] == 0
+    # the line carries the contract's keys, with the arm's own metric and workload
+    for key in ("metric", "unit", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling", "vs_baseline",
+                "dtype", "data", "config", "cpu_baseline"):
+        assert key in rec, key
+    assert rec["config"]["workload"] == "switch_tiny_f32" and rec["higher_is_better"] is True
+    assert rec["cpu_baseline"]["kind"] == "oracle" and rec["cpu_baseline"]["value"] == rec["value"]
+    assert rec["e2e"]["value"] == rec["value"] and rec["e2e"]["unit"] == rec["unit"]
