@@ -3,8 +3,9 @@
 One step = the whole hot path on one batch: router scoring + top-k + capacity
 slotting, permute, grouped SwiGLU FFN (up and down), unpermute + combine, and
 the backward (combine backward, dgrad, wgrad with fp32 accumulation, dx +
-router gradient).  Default workload: the top-2 layer (T=4096, d=1024, f=4096,
-E=8, k=2, capacity factor 1.25) in bf16 with an fp32 router.
+router gradient).  Default workload: the largest layer, dropless top-4 over 32
+experts (T=32768, d=4096, f=1536, E=32, k=4, log-Zipf 1.3 router bias) in bf16
+with an fp32 router.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -27,13 +28,17 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-DEFAULT_WORKLOAD = "top2_e8_bf16"
+DEFAULT_WORKLOAD = "dropless_e32_bf16"
 METRIC = "MoE-layer tokens/s fwd & fwd+bwd; grouped-GEMM % bf16 peak; permute GB/s"
-PROFILE_FILE = os.path.join(ROOT, "profiles", "gemm_tc_top2_e8_bf16.md")
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+# source file of each kernel kind: a committed DRAM-traffic figure is used only while its source is unchanged
 KERNEL_SOURCES = {
     "gemm_up_swiglu": "gemm_tc.cu", "gemm_down": "gemm_tc.cu", "gemm_dgrad_h_swiglu_bwd": "gemm_tc.cu",
     "gemm_dgrad_x": "gemm_tc.cu", "gemm_wgrad": "gemm_tc.cu", "permute": "rows.cu", "unpermute_combine": "rows.cu",
-    "combine_bwd": "rows.cu", "dx_router": "rows.cu", "router_topk": "routing.cu",
+    "combine_bwd": "rows.cu", "dx_router": "rows.cu", "transpose_wr": "rows.cu", "dwr_reduce": "rows.cu",
+    "router_topk": "router_tc.cu", "split_wr": "router_tc.cu", "slot_scan": "routing.cu",
+    "slot_assign": "routing.cu", "dwr": "dwr_tc.cu", "split_dl": "dwr_tc.cu", "aux_loss": "aux_loss.cu",
+    "aux_grad": "aux_loss.cu",
 }
 
 
@@ -148,24 +153,39 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- #
 # algorithmic work per kernel (per launch)
 # ----------------------------------------------------------------------------- #
-def algorithmic_work(s, N: int, accumulate: bool = True):
+def algorithmic_work(s, N: int, accumulate: bool = True, n_sms: int = 152):
     """(FLOPs, bytes) per launch of each kernel: the work the layer defines, counted on the N kept
-    assignments (pad rows excluded); bytes are each operand read once and each result written once."""
+    assignments (pad rows excluded); bytes are each operand read once and each result written once.
+    The helper kernels (weight and logit-gradient splits, scans, reductions) count the bytes their
+    step needs: their inputs read once and their outputs written once."""
     T, d, f, E, k = s.T, s.d_model, s.d_ff, s.E, s.k
     es = 2 if s.dtype == "bf16" else 4
     Wb = E * d * f * es  # one expert weight tensor
     grad_rw = 3 * E * d * f * 4 * (2 if accumulate else 1)
+    Ep = 16 if E <= 16 else (32 if E <= 32 else (64 if E <= 64 else 128))  # experts padded for the MMA
+    nb = (T + 63) // 64  # 64-token histogram blocks
+    hist = E * k * nb * 4
+    dwr_ranges = max(1, min((n_sms + d // 128 - 1) // max(1, d // 128), ((T + 63) // 64 + 1) // 2))
     return {
+        "split_wr": (0, d * E * 4 + 3 * Ep * d * 2),
         "router_topk": (2 * T * d * E, T * d * es + d * E * 4 + T * k * 8 + T * E * 4),
+        "slot_scan": (0, 2 * hist + E * 8),
+        "slot_assign": (0, T * k * 4 + hist + 2 * T * k * 4 + N * 4),
         "permute": (0, T * d * es + N * d * es),
         "gemm_up_swiglu": (4 * N * d * f, N * d * es + 2 * Wb + 3 * N * f * es),
         "gemm_down": (2 * N * f * d, N * f * es + Wb + N * d * es),
         "unpermute_combine": (0, N * d * es + T * d * es),
         "combine_bwd": (0, T * d * es + 2 * N * d * es + T * E * 4),
+        "aux_loss": (0, T * E * 4 + T * k * 4),
+        "aux_grad": (0, 3 * T * E * 4),
         "gemm_dgrad_h_swiglu_bwd": (2 * N * d * f, N * d * es + Wb + 4 * N * f * es),
         "gemm_wgrad": (6 * N * d * f, 2 * N * d * es + 3 * N * f * es + grad_rw),
         "gemm_dgrad_x": (4 * N * f * d, 2 * N * f * es + 2 * Wb + N * d * es),
+        "transpose_wr": (0, 2 * d * E * 4),
         "dx_router": (0, N * d * es + T * d * es),
+        "split_dl": (0, T * E * 4 + 3 * Ep * T * 2),
+        "dwr": (2 * T * d * E, T * d * es + T * E * 4),
+        "dwr_reduce": (0, dwr_ranges * d * E * 4 + d * E * 4 * (2 if accumulate else 1)),
     }
 
 
@@ -187,20 +207,19 @@ def source_digest(name: str) -> str:
 
 
 def committed_traffic(name: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on this
-    workload and matches the current source."""
-    if not os.path.exists(PROFILE_FILE):
+    """DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum) from the committed
+    profile of this workload, profiles/traffic_<workload>.json, when it was taken on the current
+    source of the kernel; None otherwise."""
+    path = os.path.join(PROFILE_DIR, f"traffic_{workload}.json")
+    if not os.path.exists(path):
         return None
-    vals = {}
-    for line in open(PROFILE_FILE):
-        if ":" in line and line.strip().startswith("traffic."):
-            key, v = line.strip().split(":", 1)
-            vals[key.strip()] = v.strip()
-    tb = vals.get(f"traffic.{name}.bytes_per_launch")
-    sha = vals.get(f"traffic.{name}.source_sha")
-    if tb is None or sha != source_digest(name) or vals.get("traffic.workload") != workload:
+    try:
+        rec = json.load(open(path)).get("kernels", {}).get(name)
+    except (OSError, ValueError):
         return None
-    return float(tb)
+    if not rec or rec.get("source_sha") != source_digest(name):
+        return None
+    return float(rec["dram_bytes_per_launch"])
 
 
 def peaks():
@@ -262,6 +281,17 @@ def cpu_baseline(name: str, T: int, seconds: float) -> dict:
                       f"BLAS threads = {cores}"}
 
 
+def workload_config(name: str, s) -> dict:
+    """The ``config`` of the JSON line: the same keys and values in both arms, so that the two lines
+    name one workload."""
+    return {"workload": name, "T": s.T, "d_model": s.d_model, "d_ff": s.d_ff, "E": s.E, "k": s.k,
+            "capacity_factor": s.capacity_factor, "zipf_s": s.zipf_s, "layer_dtype": s.dtype,
+            "step": "forward + backward (fp32 grad accumulate)",
+            "l2": "inputs of the GPU arm exceed L2 or a 256 MB buffer is written before every timed step, "
+                  "outside the step's events",
+            "parallelism": "data-parallel replicas, one batch per rank"}
+
+
 # ----------------------------------------------------------------------------- #
 # reference arm: the oracle as it stands
 # ----------------------------------------------------------------------------- #
@@ -284,8 +314,8 @@ def run_reference(args, world, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": len(times), "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "T": s.T, "d_model": s.d_model, "d_ff": s.d_ff, "E": s.E, "k": s.k,
-                   "capacity_factor": s.capacity_factor, "sample_tokens": tokens},
+        "config": workload_config(args.workload, s),
+        "sample_tokens": tokens,
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": f"each step: fp64 oracle forward+backward over the first {tokens} of {s.T} tokens"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -376,8 +406,8 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     fwd_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(fs, fe)), world)
 
-    # inference forward (no saved state: on bf16 layers the up product gathers
-    # its rows from x, no permuted copy), same protocol
+    # inference forward (no saved state: the permuted rows and the products live
+    # in the workspace, nothing is kept for a backward), same protocol
     Li = layer.from_workload(wl, str(dev), training=False)
     for _ in range(args.warmup):
         Li.forward(x)
@@ -462,7 +492,8 @@ def run_ours(args, world, rank, local):
 
     if rank != 0:
         return
-    work = algorithmic_work(s, N)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    work = algorithmic_work(s, N, accumulate=True, n_sms=sms)
     hbm, tflops, peak_kind = peaks()
     kernels = {}
     for name, (n, ms) in prof_all.items():
@@ -495,14 +526,10 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": s.dtype, "data": "synthetic",
-        "config": {"workload": args.workload, "T": s.T, "d_model": s.d_model, "d_ff": s.d_ff, "E": s.E, "k": s.k,
-                   "capacity_factor": s.capacity_factor, "aux_loss_coeff": args.aux_loss_coeff,
-                   "recompute": args.recompute,
-                   "kept_assignments": N,
-                   "step": "forward + backward (fp32 grad accumulate)",
-                   "l2": "256 MB buffer written before every timed step, outside the step's events",
-                   "parallelism": f"replicas x{world}",
-                   "sms": torch.cuda.get_device_properties(dev).multi_processor_count},
+        "config": workload_config(args.workload, s),
+        "run": {"aux_loss_coeff": args.aux_loss_coeff, "recompute": args.recompute, "kept_assignments": N,
+                "dropped_assignments": s.T * s.k - N, "replicas": world, "sms": sms,
+                "l2_flush": "256 MB buffer written before every timed step, outside the step's events"},
         "fwd_tokens_per_s": world * s.T * args.steps / (fwd_ms / 1e3),
         "fwd_inference_tokens_per_s": world * s.T * args.steps / (inf_ms / 1e3),
         "grouped_gemm_frac_bf16_peak": round(gemm_flops / (gemm_ms / 1e3) / 1e12 / tflops, 4) if gemm_ms else None,
@@ -512,7 +539,8 @@ def run_ours(args, world, rank, local):
         "clocks": clk,
         "kernels": kernels,
         "kernels_note": "per-kernel CUDA events from an untimed pass of min(steps, 50) steps; the timed "
-                        "region records events only around the roofline kernel",
+                        "region records events only around the roofline kernel; gbs = algorithmic bytes / "
+                        "event time (an effective rate: reads that hit L2 count as moved)",
     }
     if e2e is not None:
         line["e2e"] = e2e

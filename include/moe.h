@@ -244,8 +244,9 @@ moe_status moe_grouped_ffn_bwd(const moe_config* cfg, const void* x_perm, const 
  * probs [T, E] fp32 and ids [T, k] int32 as moe_router_topk writes them; dl
  * [T, E] fp32 is updated in place (moe_combine_bwd's output); *loss (device
  * fp32, may be NULL) receives L.  Sums run in a fixed order (bitwise
- * reproducible).  ws must hold moe_workspace_size(cfg, 1).  Does nothing when
- * the coefficient is 0. */
+ * reproducible).  ws must hold moe_workspace_size(cfg, 1).  When the
+ * coefficient is 0 (or T = 0) dl is left as it is and *loss, if given, is set
+ * to 0. */
 moe_status moe_aux_loss(const moe_config* cfg, const float* probs, const int32_t* ids, float* loss, float* dl,
                         void* ws, size_t ws_bytes, moe_stream_t stream);
 
@@ -270,19 +271,25 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* w, const void
 
 /* Bytes of device memory the library reserves, on every GPU that loads it and
  * until the process exits, for moe_router_topk_noalloc. */
-#define MOE_NOALLOC_SCRATCH_BYTES (1u << 20)
+#define MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
 
 /* moe_router_topk for callers that cannot allocate device memory: a plugin
  * hosted by a program that owns every allocation, a path whose memory budget
  * is fixed at start-up, or a latency-critical loop that cannot afford the
  * implicit device synchronisation of cudaMalloc/cudaFree.  No workspace is
- * passed; the routing histograms and scan live in a static device array of
+ * passed; the routing histograms, their scan and (bf16 layers of at least
+ * 128 tokens) the three bf16 parts of W_r live in a static device array of
  * MOE_NOALLOC_SCRATCH_BYTES owned by the library (the pages have no
  * counterpart of this entry point; it is a deployment convenience).
- * Arguments, results and errors are those of moe_router_topk, plus
- * MOE_ERR_WORKSPACE when the layer needs more than MOE_NOALLOC_SCRATCH_BYTES
- * of scratch: 2 * E * k * ceil(T/64) * 4 bytes plus a little (E = 32, k = 4
- * fits up to T = 65,000 tokens).  The call allocates nothing.
+ * It runs the same kernels as moe_router_topk for the same layer, so
+ * arguments, results (bit for bit) and errors are those of moe_router_topk,
+ * plus MOE_ERR_WORKSPACE, returned before anything is queued, when the layer
+ * needs more than MOE_NOALLOC_SCRATCH_BYTES of scratch:
+ * 2 * E * k * ceil(T/64) * 4 bytes of histograms and scan, plus
+ * 3 * E_pad * d * 2 bytes of W_r parts for bf16 layers with T >= 128
+ * (E_pad = E rounded up to 16, 32, 64 or 128), plus under 2 KB of alignment
+ * (E = 32, k = 4, d = 4096 fits up to about 210,000 tokens).  The call
+ * allocates nothing.
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture.  Every call on a device shares the one array and

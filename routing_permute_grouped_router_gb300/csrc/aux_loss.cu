@@ -113,7 +113,10 @@ size_t aux_scratch_bytes(const Shape& s) {
 
 cudaError_t launch_aux_loss(const Shape& s, float coeff, const float* probs, const int32_t* ids, float* loss,
                             float* dl, void* scratch, uint32_t* err, cudaStream_t st) {
-  if (s.T == 0 || coeff <= 0.f) return cudaSuccess;
+  if (s.T == 0 || coeff <= 0.f) {
+    // no loss term: a caller that reads the scalar every step sees 0, not a stale value
+    return loss != nullptr ? cudaMemsetAsync(loss, 0, sizeof(float), st) : cudaSuccess;
+  }
   const int nb = aux_blocks(s);
   float* part_p = static_cast<float*>(scratch);
   int32_t* part_c = reinterpret_cast<int32_t*>(part_p + (size_t)nb * s.E);

@@ -3,14 +3,18 @@
 // allocation, a fixed start-up memory budget, or a latency-critical loop that
 // cannot pay for cudaMalloc's implicit device synchronisation).
 //
-// The routing histograms, their scan and the last-block ticket live in a
-// file-scope device array owned by this library.  Host code cannot use the
-// array's name as a device address, so the first call on each device looks the
-// address up with cudaGetSymbolAddress while that device is current and keeps
-// it.  Nothing here calls cudaMalloc, cudaFree or an allocating library
-// routine.  Every call on a device shares the array and sees the previous
-// call's contents: the router kernel clears the ticket itself and every other
-// word is rewritten before it is read, but calls that overlap on the GPU race.
+// It runs the same kernels as moe_router_topk for the same layer (the
+// tensor-core router for bf16 layers of at least 128 tokens, the SIMT router
+// otherwise), so its results are bit for bit those of moe_router_topk.  The
+// routing histograms, their scan, the last-block ticket and, for the
+// tensor-core router, the three bf16 parts of W_r live in a file-scope device
+// array owned by this library.  Host code cannot use the array's name as a
+// device address, so the first call on each device looks the address up with
+// cudaGetSymbolAddress while that device is current and keeps it.  Nothing
+// here calls cudaMalloc, cudaFree or an allocating library routine.  Every
+// call on a device shares the array and sees the previous call's contents:
+// the router kernel clears the ticket itself and every other word is
+// rewritten before it is read, but calls that overlap on the GPU race.
 #include <mutex>
 
 #include "../../include/moe.h"
@@ -67,9 +71,12 @@ extern "C" moe_status moe_router_topk_noalloc(const moe_config* cfg, const void*
   if (bias != nullptr && (st = check_ptr(bias, 4)) != MOE_OK) return st;
   if (probs != nullptr && (st = check_ptr(probs, 4)) != MOE_OK) return st;
 
-  // scratch layout: hist | base (E*k*blocks ints each) | totals (E ints) | ticket
+  // scratch layout: hist | base (E*k*blocks ints each) | totals (E ints) | ticket | W_r parts (tensor-core router)
   const size_t n = (size_t)s.E * s.k * router_blocks(s.T);
-  const size_t bytes = 2 * round_up(n * 4) + round_up((size_t)s.E * 4) + round_up(4);
+  const bool tc = router_tc_supported(s);
+  const size_t o_scan = round_up(n * 4), o_totals = 2 * round_up(n * 4);
+  const size_t o_ticket = o_totals + round_up((size_t)s.E * 4), o_wsplit = o_ticket + round_up(4);
+  const size_t bytes = o_wsplit + (tc ? round_up(router_wsplit_bytes(s)) : 0);
   if (bytes > MOE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
 
   uint32_t* err = nullptr;
@@ -78,9 +85,9 @@ extern "C" moe_status moe_router_topk_noalloc(const moe_config* cfg, const void*
   if ((st = scratch_address(&base)) != MOE_OK) return st;
   char* b = static_cast<char*>(base);
   int32_t* hist = reinterpret_cast<int32_t*>(b);
-  int32_t* scan = reinterpret_cast<int32_t*>(b + round_up(n * 4));
-  int32_t* totals = reinterpret_cast<int32_t*>(b + 2 * round_up(n * 4));
-  int32_t* ticket = reinterpret_cast<int32_t*>(b + 2 * round_up(n * 4) + round_up((size_t)s.E * 4));
+  int32_t* scan = reinterpret_cast<int32_t*>(b + o_scan);
+  int32_t* totals = reinterpret_cast<int32_t*>(b + o_totals);
+  int32_t* ticket = reinterpret_cast<int32_t*>(b + o_ticket);
 
   if (s.T == 0) {
     if (cudaMemsetAsync(counts, 0, (size_t)s.E * 4, stream) != cudaSuccess ||
@@ -88,7 +95,10 @@ extern "C" moe_status moe_router_topk_noalloc(const moe_config* cfg, const void*
       return MOE_ERR_CUDA;
     return MOE_OK;
   }
-  if (launch_router(s, x, W_r, bias, ids, gates, probs, hist, ticket, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  const cudaError_t e = tc ? launch_router_tc(s, x, W_r, bias, b + o_wsplit, ids, gates, probs, hist, ticket, err,
+                                              stream)
+                           : launch_router(s, x, W_r, bias, ids, gates, probs, hist, ticket, stream);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_slot_scan(s, hist, scan, totals, ticket, counts, offsets, err, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (launch_slot_assign(s, ids, scan, counts, offsets, slot, row_of, src_token, err, stream) != cudaSuccess)

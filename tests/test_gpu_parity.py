@@ -317,8 +317,8 @@ def test_permute_then_unpermute_is_identity_on_gpu(k):
                                    LS("inf_cap0", 200, 256, 256, 4, 2, 1.0, W.BF16, capacity=0),
                                    LS("inf_e128_k8", 300, 256, 256, 128, 8, 1.0, W.BF16)])
 def test_inference_forward(shape):
-    """Forward without saved state: on bf16 layers the up product gathers its rows
-    from x through src_token (no permuted copy); y must match the oracle."""
+    """Forward without saved state (permuted rows and products in the workspace,
+    nothing kept for a backward); y must match the oracle."""
     wl = W.make(shape, seed=12, micro_batches=1, with_dy=False)
     L = layer.from_workload(wl, training=False)
     y = L.forward(wl.x[0].torch("cuda"))
@@ -329,12 +329,16 @@ def test_inference_forward(shape):
 
 
 @pytest.mark.parametrize("name", ["train_e16_small", "top2_e8_small", "train_f32_small"])
-def test_recompute_variant_is_bitwise_the_saving_path(name):
+def test_recompute_variant_matches_oracle_and_the_saving_path(name):
     """Keeping neither a, b nor h (the backward recomputes them with the same up
-    product) gives y, dx and every gradient bit for bit as the layer that keeps
-    them, over two accumulated micro-batches."""
+    product): y, dx and every gradient over two accumulated micro-batches match
+    the oracle's training step at the layer's tolerance, and bit for bit the
+    layer that keeps them."""
     s = SMALL[name]
+    tol = TOL[s.dtype]
     wl = W.make(s, seed=21, micro_batches=2, with_dy=True)
+    ref = O.train_step([x.f64() for x in wl.x], [dy.f64() for dy in wl.dy], wl.W_r, wl.bias, wl.W1.f64(),
+                       wl.W3.f64(), wl.W2.f64(), s.k, _cap(s))
     res = []
     for recompute in (False, True):
         L = layer.from_workload(wl, recompute=recompute)
@@ -346,7 +350,13 @@ def test_recompute_variant_is_bitwise_the_saving_path(name):
             L.backward(x, dy, accumulate=m > 0)
             torch.cuda.synchronize()
             check_no_device_error()
+            st, gr = ref["micro_batches"][m]
+            assert_routing_equal(L.saved, st, s.T)
+            assert_close(f"y[{m}] recompute={recompute}", L.y[: s.T], st["y"], tol)
+            assert_close(f"dx[{m}] recompute={recompute}", L.dx[: s.T], gr["dx"], tol)
             out += [L.y[: s.T].clone(), L.dx[: s.T].clone()]
+        for n in ("dW_r", "dW1", "dW3", "dW2"):
+            assert_close(f"{n} recompute={recompute}", L.grads[n], ref["grads"][n], tol)
         out += [L.grads[n].clone() for n in ("dW_r", "dW1", "dW3", "dW2")]
         res.append(out)
     for u, v in zip(*res):

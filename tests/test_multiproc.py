@@ -74,5 +74,11 @@ def test_reference_arm_under_torchrun_prints_once():
                 "dtype", "data", "config", "cpu_baseline"):
         assert key in rec, key
     assert rec["config"]["workload"] == "switch_tiny_f32" and rec["higher_is_better"] is True
+    # the same config dict as the GPU arm builds for this workload, key for key
+    sys.path.insert(0, ROOT)
+    import bench
+    from routing_permute_grouped_router_gb300 import workload as W
+
+    assert rec["config"] == bench.workload_config("switch_tiny_f32", W.WORKLOADS["switch_tiny_f32"])
     assert rec["cpu_baseline"]["kind"] == "oracle" and rec["cpu_baseline"]["value"] == rec["value"]
     assert rec["e2e"]["value"] == rec["value"] and rec["e2e"]["unit"] == rec["unit"]
