@@ -165,7 +165,8 @@ def algorithmic_work(s, N: int, accumulate: bool = True, n_sms: int = 152):
     Ep = 16 if E <= 16 else (32 if E <= 32 else (64 if E <= 64 else 128))  # experts padded for the MMA
     nb = (T + 63) // 64  # 64-token histogram blocks
     hist = E * k * nb * 4
-    dwr_ranges = max(1, min((n_sms + d // 128 - 1) // max(1, d // 128), ((T + 63) // 64 + 1) // 2))
+    dwr_blocks = max(1, d // (256 if Ep <= 64 else 128))  # CTAs of the router-weight gradient along d
+    dwr_ranges = max(1, min(n_sms // dwr_blocks, ((T + 63) // 64 + 1) // 2))
     return {
         "split_wr": (0, d * E * 4 + 3 * Ep * d * 2),
         "router_topk": (2 * T * d * E, T * d * es + d * E * 4 + T * k * 8 + T * E * 4),
@@ -182,7 +183,7 @@ def algorithmic_work(s, N: int, accumulate: bool = True, n_sms: int = 152):
         "gemm_wgrad": (6 * N * d * f, 2 * N * d * es + 3 * N * f * es + grad_rw),
         "gemm_dgrad_x": (4 * N * f * d, 2 * N * f * es + 2 * Wb + N * d * es),
         "transpose_wr": (0, 2 * d * E * 4),
-        "dx_router": (0, N * d * es + T * d * es),
+        "dx_router": (0, N * d * es + T * d * es + T * E * 4),
         "split_dl": (0, T * E * 4 + 3 * Ep * T * 2),
         "dwr": (2 * T * d * E, T * d * es + T * E * 4),
         "dwr_reduce": (0, dwr_ranges * d * E * 4 + d * E * 4 * (2 if accumulate else 1)),

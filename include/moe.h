@@ -331,6 +331,13 @@ int32_t moe_kernel_kinds(void);
  * launches issued after the call; records already taken are kept. */
 moe_status moe_profiler_filter(int32_t id);
 const char* moe_kernel_name(int32_t id);
+/* NVTX ranges for timeline tools (off by default; the pages have no
+ * counterpart).  While on, every kernel launch is bracketed by an NVTX range
+ * named after its kernel kind (moe_kernel_name) and every moe_layer_fwd /
+ * moe_layer_bwd call by a range of that name, pushed and popped on the
+ * calling host thread, so an nsys or ncu timeline can be cut by layer step and
+ * kernel.  Without a tool attached a range costs a few nanoseconds.  Host only. */
+moe_status moe_nvtx_enable(int on);
 moe_status moe_profiler_read(int32_t id, int64_t* launches, double* total_ms);
 
 #ifdef __cplusplus

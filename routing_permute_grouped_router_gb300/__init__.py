@@ -80,6 +80,7 @@ _SIGNATURES = {
     "moe_profiler_enable": [_I],
     "moe_kernel_kinds": [],
     "moe_profiler_filter": [ctypes.c_int32],
+    "moe_nvtx_enable": [_I],
     "moe_kernel_name": [ctypes.c_int32],
     "moe_profiler_read": [ctypes.c_int32, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double)],
     "moe_status_string": [_I],
@@ -285,6 +286,11 @@ def moe_profiler_filter(name: Optional[str]) -> None:
         names = [lib().moe_kernel_name(i).decode() for i in range(lib().moe_kernel_kinds())]
         idx = names.index(name)
     _check("moe_profiler_filter", lib().moe_profiler_filter(idx))
+
+
+def moe_nvtx_enable(on: bool) -> None:
+    """NVTX ranges around every kernel launch and layer call (for nsys/ncu timelines)."""
+    _check("moe_nvtx_enable", lib().moe_nvtx_enable(int(bool(on))))
 
 
 def moe_profiler_read() -> dict:

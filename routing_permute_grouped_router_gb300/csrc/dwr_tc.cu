@@ -12,11 +12,17 @@
 //
 // split_dl_kernel writes the parts transposed, [3][E_pad][T_pitch] bf16, so
 // that each part is a K-major MMA operand with 128-byte rows.  dwr_tc_kernel
-// takes a 128-row block of d (M) and one of S contiguous ranges of T (K):
-// warp 0 lane 0 loads x^T (MN-major, two 64 x 64 boxes) and the three dl
-// parts with TMA, warp 1 lane 0 issues tcgen05.mma (M=128, N=E_pad, K=16)
-// into an fp32 TMEM accumulator, and warps 2-5 write the 128 x E partial to
-// partial[range][d][E].  The ranges are then added in range order
+// takes MT consecutive 128-row blocks of d (M; MT = 2 up to 64 experts) and one
+// of S contiguous ranges of T (K): warp 0 lane 0 loads x^T (MN-major, two
+// 64 x 64 boxes per block, so each token row is read in MT * 256-byte runs)
+// and the three dl parts once per stage with TMA; the parts land as
+// consecutive E_pad-row blocks, so together they are one K-major operand of
+// 3 * E_pad rows, and warp 1 lane 0 issues one tcgen05.mma (M=128,
+// N=3*E_pad, K=16; two MMAs of 256 and 128 columns when E_pad = 128) per block
+// and K step against them into MT fp32 TMEM accumulators of three column
+// groups (x^T hi, x^T mid, x^T lo); warps 2-5 add each row's three groups,
+// lo + mid first, and write the (MT * 128) x E partial to partial[range][d][E].  The grid is one wave (at
+// most one CTA per SM).  The ranges are then added in range order
 // (dwr_reduce_kernel), so the result does not depend on timing.
 #include <cudaTypedefs.h>
 
@@ -26,22 +32,36 @@
 namespace moe {
 namespace {
 
-constexpr int DM = 128;  // rows of d per tile
+constexpr int DM = 128;  // rows of d per MMA block
 constexpr int DK = 64;   // tokens per stage (128-byte rows)
 constexpr int D_THREADS = 192;
+constexpr int D_SMEM_MAX = 232448;  // 227 KB per CTA
 
+// MT 128-row blocks of d per CTA: two while the staged dl parts are small, so a
+// stage's dl parts serve twice the MMA work and x is read in 512-byte runs.
 template <int N>
 struct DCfg {
-  static constexpr int A_BYTES = DM * DK * 2;       // x^T block: two 64 x 64 boxes
+  static constexpr int MT = N <= 64 ? 2 : 1;
+  static constexpr int A_BYTES = MT * DM * DK * 2;  // x^T: two 64 x 64 boxes per block
   static constexpr int B_BYTES = 3 * N * DK * 2;    // the three dl parts
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int NST = N <= 32 ? 6 : (N <= 64 ? 4 : 3);
+  static constexpr int NST0 = (D_SMEM_MAX - 256 - 1024) / STAGE;
+  static constexpr int NST = NST0 > 6 ? 6 : NST0;
   static constexpr int CTRL_OFF = NST * STAGE;
   static constexpr int SMEM = CTRL_OFF + 256 + 1024;
-  static constexpr uint32_t TCOLS = N < 32 ? 32 : N;
-  // fp32 D, bf16 A (MN-major) and B (K-major), M = 128, N
-  static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) |
-                                    ((uint32_t)(N >> 3) << 17) | ((uint32_t)(DM >> 4) << 24);
+  // accumulator columns per block: the three parts side by side
+  static constexpr int NS = 3 * N;
+  static constexpr uint32_t TCOLS = MT * NS <= 32 ? 32 : (MT * NS <= 64 ? 64 : (MT * NS <= 128 ? 128 : (MT * NS <= 256 ? 256 : 512)));
+  static_assert(MT * NS <= 512, "TMEM columns");
+  static_assert(NST >= 2 && SMEM <= D_SMEM_MAX, "shared memory budget");
+  // MMA widths: one of 3 * E_pad columns, or 256 + 128 for E_pad = 128
+  static constexpr int N0 = NS <= 256 ? NS : 256;
+  static constexpr int N1 = NS - N0;
+  // fp32 D, bf16 A (MN-major) and B (K-major), M = 128, N = n
+  static constexpr uint32_t IDESC0 =
+      (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | ((uint32_t)(N0 >> 3) << 17) | ((uint32_t)(DM >> 4) << 24);
+  static constexpr uint32_t IDESC1 = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) |
+                                     ((uint32_t)((N1 > 0 ? N1 : 16) >> 3) << 17) | ((uint32_t)(DM >> 4) << 24);
 };
 
 // dl [T, E] fp32 -> parts [3][N][tp] bf16 (rows e >= E and columns t >= T are
@@ -94,7 +114,7 @@ __global__ void __launch_bounds__(D_THREADS, 1) dwr_tc_kernel(const __grid_const
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int m0 = blockIdx.x * DM, range = blockIdx.y;
+  const int m0 = blockIdx.x * (C::MT * DM), range = blockIdx.y;
   const int kb0 = range * a.kall / a.S, kb1 = (range + 1) * a.kall / a.S;
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NST; ++i) {
@@ -132,8 +152,8 @@ __global__ void __launch_bounds__(D_THREADS, 1) dwr_tc_kernel(const __grid_const
         const uint32_t fb = smem_addr(&full_bar[stage]);
         mbar_expect_tx(fb, C::STAGE);
         const uint32_t sA = smem_base + stage * C::STAGE;
-        tma_load_2d(sA, &map_x, fb, m0, kb * DK);
-        tma_load_2d(sA + 8192, &map_x, fb, m0 + 64, kb * DK);
+#pragma unroll
+        for (int b = 0; b < 2 * C::MT; ++b) tma_load_2d(sA + b * 8192, &map_x, fb, m0 + 64 * b, kb * DK);
 #pragma unroll
         for (int p = 0; p < 3; ++p) tma_load_2d(sA + C::A_BYTES + p * N * 128, &map_l, fb, kb * DK, p * N);
         ++issued;
@@ -171,11 +191,15 @@ __global__ void __launch_bounds__(D_THREADS, 1) dwr_tc_kernel(const __grid_const
         const uint32_t sB = sA + C::A_BYTES;
 #pragma unroll
         for (int k16 = 0; k16 < DK / 16; ++k16) {
-          const uint64_t ad = sdesc(sA + k16 * 2048, 8192, 1024);
+          const uint32_t acc = (kb != kb0 || k16 != 0) ? 1u : 0u;
 #pragma unroll
-          for (int p = 0; p < 3; ++p)
-            umma_bf16(tmem_base, ad, sdesc(sB + p * N * 128 + k16 * 32, 16, 1024), C::IDESC,
-                      (kb != kb0 || k16 != 0 || p != 0) ? 1u : 0u);
+          for (int mt = 0; mt < C::MT; ++mt) {
+            const uint64_t ad = sdesc(sA + mt * (DM * DK * 2) + k16 * 2048, 8192, 1024);
+            umma_bf16(tmem_base + mt * C::NS, ad, sdesc(sB + k16 * 32, 16, 1024), C::IDESC0, acc);
+            if (C::N1 > 0)
+              umma_bf16(tmem_base + mt * C::NS + C::N0, ad, sdesc(sB + C::N0 * 128 + k16 * 32, 16, 1024),
+                        C::IDESC1, acc);
+          }
         }
         umma_commit(smem_addr(&empty_bar[stage]));
         if (++stage == C::NST) {
@@ -189,20 +213,29 @@ __global__ void __launch_bounds__(D_THREADS, 1) dwr_tc_kernel(const __grid_const
       }
     }
   } else {
-    // ---- epilogue: one row of d per thread ----
+    // ---- epilogue: one row of d per thread and block ----
     const int q = warp & 3;
-    const int row = m0 + q * 32 + lane;
     if (mbar_wait(smem_addr(tfull_bar), 0, abort_flag, a.err, 652)) {
       tc_fence_after();
-      float* dst = a.partial + ((size_t)range * a.d + row) * a.E;
 #pragma unroll
-      for (int c = 0; c < N / 16; ++c) {
-        uint32_t r[16];
-        tmem_ld16(tmem_base + ((uint32_t)(q * 32) << 16) + c * 16, r);
-        tmem_ld_wait16(r);
+      for (int mt = 0; mt < C::MT; ++mt) {
+        const int row = m0 + mt * DM + q * 32 + lane;
+        float* dst = a.partial + ((size_t)range * a.d + row) * a.E;
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          if (c * 16 + i < a.E) dst[c * 16 + i] = __uint_as_float(r[i]);
+        for (int c = 0; c < N / 16; ++c) {
+          uint32_t hi[16], mid[16], lo[16];
+          const uint32_t col = tmem_base + ((uint32_t)(q * 32) << 16) + mt * C::NS + c * 16;
+          tmem_ld16(col, hi);
+          tmem_ld16(col + N, mid);
+          tmem_ld16(col + 2 * N, lo);
+          tmem_ld_wait16(hi);
+          tmem_reg_fence16(mid);
+          tmem_reg_fence16(lo);
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (c * 16 + i < a.E)
+              dst[c * 16 + i] = (__uint_as_float(lo[i]) + __uint_as_float(mid[i])) + __uint_as_float(hi[i]);
+        }
       }
     }
   }
@@ -269,19 +302,21 @@ cudaError_t launch_dwr_n(const CUtensorMap& mx, const CUtensorMap& ml, const Dwr
     attr_done[dev] = true;
   }
   LaunchScope ls(KK_DWR, st);
-  return launch_pdl(dwr_tc_kernel<N>, dim3(args.d / DM, args.S), dim3(D_THREADS), (size_t)DCfg<N>::SMEM, st, mx, ml,
-                    args);
+  return launch_pdl(dwr_tc_kernel<N>, dim3(args.d / (DCfg<N>::MT * DM), args.S), dim3(D_THREADS),
+                    (size_t)DCfg<N>::SMEM, st, mx, ml, args);
 }
 
 }  // namespace
 
-bool dwr_tc_supported(const Shape& s) { return s.bf16 && s.d % DM == 0 && s.E <= 128 && s.T > 0; }
+int dwr_mt(const Shape& s) { return pad_experts(s.E) <= 64 ? 2 : 1; }
 
-// Ranges of T: about one CTA per SM over the d blocks, each range at least
-// two k-blocks of 64 tokens.
+bool dwr_tc_supported(const Shape& s) { return s.bf16 && s.d % (dwr_mt(s) * DM) == 0 && s.E <= 128 && s.T > 0; }
+
+// Ranges of T: as many as keep the grid within one wave (one CTA per SM over
+// the blocks of d), each range at least two k-blocks of 64 tokens.
 int dwr_tc_ranges(const Shape& s) {
-  const int mt = s.d / DM, kall = (s.T + DK - 1) / DK;
-  int S = (sms() + mt - 1) / mt;
+  const int mt = s.d / (dwr_mt(s) * DM), kall = (s.T + DK - 1) / DK;
+  int S = sms() / (mt > 0 ? mt : 1);
   const int most = (kall + 1) / 2;
   if (S > most) S = most;
   return S < 1 ? 1 : S;

@@ -7,6 +7,8 @@
 //
 //   UP      [a | b] = X_e [W1_e | W3_e]   -> h = silu(a) * b (and a, b)   A K-major, B MN-major
 //   DOWN    y_perm  = H_e W2_e                                            A K-major, B MN-major
+//   DOWN_COMBINE  y[t] += g * (H_e W2_e)[row] for the token t of each row (the
+//           inference forward at k <= 2: the combine in the epilogue)      A K-major, B MN-major
 //   DGRAD_H dH = dY_e W2_e^T -> da, db (SwiGLU backward in the epilogue)  A K-major, B K-major
 //   DGRAD_X dx_perm = [da | db] [W1_e | W3_e]^T (K concatenated)          A K-major, B K-major
 //   WGRAD   dW1_e = X_e^T da, dW3_e = X_e^T db, dW2_e = H_e^T dY_e (fp32)  A MN-major, B MN-major
@@ -58,7 +60,7 @@ constexpr int MAX_SMEM = 232448;  // 227 KB per CTA
 constexpr int MAX_ST = 6;
 constexpr int WG_AHEAD = 2;  // wgrad: old-gradient boxes requested ahead of the one being added
 
-enum Mode { M_UP = 0, M_DOWN = 1, M_DGRAD_H = 2, M_DGRAD_X = 3, M_WGRAD = 4 };
+enum Mode { M_UP = 0, M_DOWN = 1, M_DGRAD_H = 2, M_DGRAD_X = 3, M_WGRAD = 4, M_DOWN_COMB = 5 };
 
 // Pipeline depth and epilogue staging per product.  Each epilogue warp owns two
 // output boxes (double buffering of its TMA stores).  dgrad h also stages its a
@@ -104,6 +106,9 @@ struct TcArgs {
   float* w0;  // WGRAD: dW1
   float* w1;  // WGRAD: dW3
   float* w2;  // WGRAD: dW2
+  const int32_t* src_token;  // DOWN_COMBINE: token of each row (-1: pad row)
+  const float* row_gate;     // DOWN_COMBINE: gate of each row
+  __nv_bfloat16* y;          // DOWN_COMBINE: [T, d] output, zeroed beforehand
   int accumulate;
   uint32_t* err;
 };
@@ -180,11 +185,35 @@ struct Tile {
 template <int MODE>
 __device__ __forceinline__ int n_tiles_of(const TcArgs& a) {
   if (MODE == M_UP) return a.f / 128;
-  if (MODE == M_DOWN || MODE == M_DGRAD_X) return a.d / BN;
+  if (MODE == M_DOWN || MODE == M_DOWN_COMB || MODE == M_DGRAD_X) return a.d / BN;
   return a.f / BN;  // DGRAD_H
 }
 
-// s_pair[e]: pair tiles (of 2 x 128 rows) before expert e in the ragged-M modes.
+// The j-th tile of pair `pair`, or -1 past the last one.  Tiles are dealt
+// round-robin.  When WGRAD's experts differ widely in rows (`interleave`), it
+// lists its tiles by expert from the most rows to the fewest (s_pair holds
+// that expert order) and deals them from both ends of the list: the pair takes
+// two consecutive places of a round, and place m is the (m / 2)-th tile from
+// the front when m is even, from the back when odd.  Each pair so alternates a
+// long, tensor-bound tile with a short one whose fp32 gradient
+// read-modify-write is HBM-bound, and the short tile's epilogue runs under the
+// next long tile's mainloop instead of in a separate tail.  With experts of
+// similar size the plain order keeps the tiles running together on one
+// expert's rows, which share L2.
+template <int MODE>
+__device__ __forceinline__ int sched_tile(int j, int pair, int npairs, int total, bool interleave) {
+  if (MODE != M_WGRAD || !interleave) {
+    const int tile = pair + j * npairs;
+    return tile < total ? tile : -1;
+  }
+  const int m = (j >> 1) * 2 * npairs + 2 * pair + (j & 1);
+  if (m >= total) return -1;
+  return (m & 1) ? total - 1 - (m >> 1) : (m >> 1);
+}
+
+// s_pair[e]: pair tiles (of 2 x 128 rows) before expert e in the ragged-M modes;
+// WGRAD: s_pair[r] is the r-th expert of the tile list (the expert with the
+// r-th most rows, ties to the lower index, when interleaving; else r).
 template <int MODE>
 __device__ __forceinline__ Tile decode(int tile, uint32_t rank, const TcArgs& a, const int* s_off, const int* s_cnt,
                                        const int* s_pair) {
@@ -192,7 +221,7 @@ __device__ __forceinline__ Tile decode(int tile, uint32_t rank, const TcArgs& a,
   t.valid = true;
   if (MODE == M_WGRAD) {
     const int P = (a.d / (2 * BM)) * (a.f / BN);  // pair tiles of one product of one expert
-    t.e = tile / (3 * P);
+    t.e = s_pair[tile / (3 * P)];
     const int q = tile % (3 * P);
     int r, nt;
     if (q < 2 * P) {
@@ -227,7 +256,7 @@ __device__ __forceinline__ Tile decode(int tile, uint32_t rank, const TcArgs& a,
     const int local = 2 * (l % pe) + (int)rank;
     t.valid = local < (s_off[t.e + 1] - s_off[t.e]) / BM;
     t.row0 = (int64_t)s_off[t.e] + (int64_t)local * BM;
-    const int K = (MODE == M_UP || MODE == M_DGRAD_H) ? a.d : (MODE == M_DOWN ? a.f : 2 * a.f);
+    const int K = (MODE == M_UP || MODE == M_DGRAD_H) ? a.d : ((MODE == M_DOWN || MODE == M_DOWN_COMB) ? a.f : 2 * a.f);
     t.kblocks = K / BK;
   }
   return t;
@@ -251,7 +280,7 @@ __device__ __forceinline__ void issue_stage(const TcMaps& maps, const TcArgs& a,
     const int wr = t.e * a.d + kb * BK;
     ld(sB, bm, t.n0, wr);
     ld(sB + 8192, bm, t.n0 + 64, wr);
-  } else if (MODE == M_DOWN) {
+  } else if (MODE == M_DOWN || MODE == M_DOWN_COMB) {
     ld(sA, &maps.m[0], kb * BK, r0);
     const int wr = t.e * a.f + kb * BK;
     ld(sB, &maps.m[1], t.n0 + nh, wr);
@@ -392,6 +421,33 @@ __device__ __forceinline__ bool epilogue_tile(const TcMaps& maps, const TcArgs& 
         }
         box_issue_store(&maps.m[4 + which], buf, t.n0 + c * 64, row0, lane);
         ++es.nbox;
+      }
+    }
+  } else if (MODE == M_DOWN_COMB) {
+    // each lane owns one row: scale it by its gate and add it into its token's
+    // row of y, 16 bytes (eight bf16) per reduction.  A token has at most two
+    // kept rows, and two additions onto a zero commute, so y does not depend
+    // on which of its rows lands first.
+    const int64_t row = (int64_t)row0 + lane;
+    const int tok = row < a.max_rows ? a.src_token[row] : -1;
+    const float g = tok >= 0 ? a.row_gate[row] : 0.f;
+    __nv_bfloat16* yrow = a.y + (int64_t)(tok >= 0 ? tok : 0) * a.d + t.n0;
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+      uint32_t r[32];
+      tmem_ld32(tacc + c * 32, r);
+      tmem_ld_wait(r);
+      if (tok >= 0) {
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {
+          float w[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) w[i] = g * __uint_as_float(r[8 * q8 + i]);
+          const uint4 v = pack(w);
+          asm volatile("red.global.add.noftz.v4.bf16x2 [%0], {%1, %2, %3, %4};" ::"l"(yrow + c * 32 + q8 * 8),
+                       "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                       : "memory");
+        }
       }
     }
   } else if (MODE == M_DOWN || MODE == M_DGRAD_X) {
@@ -535,6 +591,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(load_bar + 4 * EPI_WARPS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_total = reinterpret_cast<int*>(tmem_slot + 2);
+  int* s_interleave = reinterpret_cast<int*>(tmem_slot + 3);
   int* s_off = reinterpret_cast<int*>(ctrl + 320);  // E + 1 ints
   int* s_cnt = s_off + MAX_E + 1;                   // E ints
   int* s_pair = s_cnt + MAX_E;                      // E + 1 ints
@@ -561,6 +618,15 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
   for (int i = threadIdx.x; i <= a.E; i += THREADS) s_off[i] = a.offsets[i];
   for (int i = threadIdx.x; i < a.E; i += THREADS) s_cnt[i] = a.counts[i];
   __syncthreads();
+  if (MODE == M_WGRAD) {
+    // experts ordered by rows, most first (the rank of each expert, computed in parallel)
+    for (int e = threadIdx.x; e < a.E; e += THREADS) {
+      int r = 0;
+      for (int o = 0; o < a.E; ++o) r += (s_cnt[o] > s_cnt[e]) || (s_cnt[o] == s_cnt[e] && o < e);
+      s_pair[r] = e;
+    }
+    __syncthreads();
+  }
   cluster_sync();  // the peer's barriers exist before any arrival crosses the pair
   if (warp == 1) {
     tmem_alloc_pair(smem_addr(tmem_slot), TMEM_COLS);
@@ -582,9 +648,17 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
       ok = len >= 0 && (s_off[e] & (BM - 1)) == 0 && s_cnt[e] >= 0 && s_cnt[e] <= len;
     }
     int total = 0;
+    *s_interleave = 0;
     if (ok && same_tmem) {
       if (MODE == M_WGRAD) {
         total = a.E * 3 * (a.d / (2 * BM)) * (a.f / BN);
+        // interleave long and short tiles only when some tiles are long (at least
+        // 64 k-blocks) and the experts' rows differ at least eightfold
+        const int kb_most = (s_cnt[s_pair[0]] + BK - 1) / BK, kb_least = (s_cnt[s_pair[a.E - 1]] + BK - 1) / BK;
+        const bool il = kb_most >= 64 && kb_most >= 8 * (kb_least > 0 ? kb_least : 1);
+        *s_interleave = il ? 1 : 0;
+        if (!il)
+          for (int r = 0; r < a.E; ++r) s_pair[r] = r;
       } else {
         s_pair[0] = 0;
         for (int e = 0; e < a.E; ++e) s_pair[e + 1] = s_pair[e] + ((s_off[e + 1] - s_off[e]) / BM + 1) / 2;
@@ -597,6 +671,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
   }
   __syncthreads();
   const int total = *s_total;
+  const bool interleave = *s_interleave != 0;
   const uint32_t tmem_base = *tmem_slot;
   const uint32_t smem_base = smem_addr(smem);
 
@@ -609,7 +684,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
       uint32_t phase = 0;
       int issued = 0;
       bool alive = true;
-      for (int tile = pair; tile < total && alive; tile += npairs) {
+      int tile;
+      for (int j = 0; (tile = sched_tile<MODE>(j, pair, npairs, total, interleave)) >= 0 && alive; ++j) {
         const Tile t = decode<MODE>(tile, rank, a, s_off, s_cnt, s_pair);
         for (int kb = 0; kb < t.kblocks; ++kb) {
           if (!mbar_wait(smem_addr(&empty_bar[stage]), phase ^ 1u, abort_flag, a.err, 100 + MODE)) {
@@ -656,13 +732,14 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
     if (lane == 0 && rank == 0) {
       // ---------------- MMA issuer (first CTA of the pair) ----------------
       constexpr bool A_MN = MODE == M_WGRAD;
-      constexpr bool B_MN = MODE == M_UP || MODE == M_DOWN || MODE == M_WGRAD;
+      constexpr bool B_MN = MODE == M_UP || MODE == M_DOWN || MODE == M_DOWN_COMB || MODE == M_WGRAD;
       constexpr uint32_t IDESC = idesc_bf16(A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
       bool alive = true;
-      for (int tile = pair; tile < total && alive; tile += npairs, ++local) {
+      int tile;
+      for (int j = 0; (tile = sched_tile<MODE>(j, pair, npairs, total, interleave)) >= 0 && alive; ++j, ++local) {
         const Tile t = decode<MODE>(tile, rank, a, s_off, s_cnt, s_pair);
         const int acc = local % ACC_BUFS;
         const uint32_t use = (uint32_t)(local / ACC_BUFS) & 1u;
@@ -707,7 +784,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
     const uint32_t lbar = smem_addr(&load_bar[4 * ew]);
     EpiState es{0u, {0u, 0u, 0u, 0u}, {false, false, false, false}};
     int local = 0;
-    for (int tile = pair; tile < total; tile += npairs, ++local) {
+    int tile;
+    for (int j = 0; (tile = sched_tile<MODE>(j, pair, npairs, total, interleave)) >= 0; ++j, ++local) {
       const Tile t = decode<MODE>(tile, rank, a, s_off, s_cnt, s_pair);
       const int acc = local % ACC_BUFS;
       const uint32_t use = (uint32_t)(local / ACC_BUFS) & 1u;
@@ -856,7 +934,9 @@ cudaError_t tc_ffn_fwd(const Shape& s, const FfnFwdArgs& f, uint32_t* err, cudaS
             make_map(&up.m[2], f.W3, E * d, ff, 64, 64) && make_map(&up.m[3], f.h, R, ff, 64, 32);
   if (f.a != nullptr) ok = ok && make_map(&up.m[4], f.a, R, ff, 64, 32);
   if (f.b != nullptr) ok = ok && make_map(&up.m[5], f.b, R, ff, 64, 32);
-  if (f.y_perm != nullptr)  // null: the up product alone (the backward's recompute)
+  if (f.y_comb != nullptr)  // the down product adds into y (inference forward, k <= 2)
+    ok = ok && make_map(&down.m[0], f.h, R, ff, 64, BM) && make_map(&down.m[1], f.W2, E * ff, d, 64, 64);
+  else if (f.y_perm != nullptr)  // null: the up product alone (the backward's recompute)
     ok = ok && make_map(&down.m[0], f.h, R, ff, 64, BM) && make_map(&down.m[1], f.W2, E * ff, d, 64, 64) &&
          make_map(&down.m[2], f.y_perm, R, d, 64, 32);
   if (!ok) return cudaErrorInvalidValue;
@@ -865,7 +945,15 @@ cudaError_t tc_ffn_fwd(const Shape& s, const FfnFwdArgs& f, uint32_t* err, cudaS
   a.o1 = static_cast<__nv_bfloat16*>(f.a);
   a.o2 = static_cast<__nv_bfloat16*>(f.b);
   cudaError_t e = launch_mode<M_UP>(up, a, mp * (s.f / 128), KK_GEMM_UP, st);
-  if (e != cudaSuccess || f.y_perm == nullptr) return e;
+  if (e != cudaSuccess) return e;
+  if (f.y_comb != nullptr) {
+    a.o1 = a.o2 = nullptr;
+    a.src_token = f.src_token;
+    a.row_gate = f.row_gate;
+    a.y = static_cast<__nv_bfloat16*>(f.y_comb);
+    return launch_mode<M_DOWN_COMB>(down, a, mp * (s.d / BN), KK_GEMM_DOWN, st);
+  }
+  if (f.y_perm == nullptr) return e;
   a.o0 = static_cast<__nv_bfloat16*>(f.y_perm);
   a.o1 = a.o2 = nullptr;
   return launch_mode<M_DOWN>(down, a, mp * (s.d / BN), KK_GEMM_DOWN, st);

@@ -83,8 +83,11 @@ cudaError_t launch_router_tc(const Shape& s, const void* x, const float* W_r, co
                              uint32_t* err, cudaStream_t st);
 
 // ---- rows.cu ----
+// With y_zero and row_gate given it also zeroes y_zero[t] and writes
+// row_gate[row_of[t,j]] = gates[t,j] (the combine fused into the down product).
 cudaError_t launch_permute(const Shape& s, const void* x, const int32_t* row_of, const int32_t* counts,
-                           const int32_t* offsets, void* x_perm, uint32_t* err, cudaStream_t st);
+                           const int32_t* offsets, void* x_perm, uint32_t* err, cudaStream_t st,
+                           const float* gates = nullptr, float* row_gate = nullptr, void* y_zero = nullptr);
 cudaError_t launch_combine(const Shape& s, const void* y_perm, const int32_t* row_of, const float* gates, void* y,
                            uint32_t* err, cudaStream_t st);
 cudaError_t launch_combine_bwd(const Shape& s, const void* dy, const void* y_perm, const int32_t* ids,
@@ -119,6 +122,9 @@ struct FfnFwdArgs {
   const void* x_perm; const int32_t* counts; const int32_t* offsets;
   const void* W1; const void* W3; const void* W2;
   void* h; void* y_perm; void* a; void* b;  // y_perm null: the up product only
+  // bf16 only: with y_comb set the down product adds row_gate[row] * its row into
+  // y_comb[src_token[row]] (zeroed beforehand) instead of writing y_perm
+  const int32_t* src_token = nullptr; const float* row_gate = nullptr; void* y_comb = nullptr;
 };
 struct FfnBwdArgs {
   const void* x_perm; const void* a; const void* b; const void* h; const void* dy_perm;

@@ -8,6 +8,8 @@
 #include <mutex>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/moe.h"
 #include "internal.h"
 
@@ -62,6 +64,9 @@ int g_prof_filter = -1;
 std::vector<ProfRec> g_prof_recs;
 std::vector<cudaEvent_t> g_event_pool;
 thread_local int t_open_rec = -1;
+// NVTX ranges around every launch and layer call, for nsys/ncu timelines
+std::atomic<bool> g_nvtx{false};
+thread_local bool t_nvtx_open = false;
 
 cudaEvent_t pool_event() {
   if (!g_event_pool.empty()) {
@@ -84,6 +89,8 @@ const char* const kKernelNames[KK_COUNT] = {
 
 void launch_begin(int kind, cudaStream_t s) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
+  t_nvtx_open = g_nvtx.load(std::memory_order_relaxed);
+  if (t_nvtx_open) nvtxRangePushA(kKernelNames[kind]);
   std::lock_guard<std::mutex> lk(g_prof_mu);
   if (!g_prof_on || (g_prof_filter >= 0 && g_prof_filter != kind)) {
     t_open_rec = -1;
@@ -97,12 +104,25 @@ void launch_begin(int kind, cudaStream_t s) {
 
 void launch_end(int kind, cudaStream_t s) {
   (void)kind;
+  if (t_nvtx_open) nvtxRangePop();
+  t_nvtx_open = false;
   std::lock_guard<std::mutex> lk(g_prof_mu);
   if (t_open_rec >= 0 && t_open_rec < (int)g_prof_recs.size()) cudaEventRecord(g_prof_recs[t_open_rec].b, s);
   t_open_rec = -1;
 }
 
 namespace {
+
+// An NVTX range over a whole layer call while NVTX ranges are on.
+struct NvtxScope {
+  bool on;
+  explicit NvtxScope(const char* name) : on(g_nvtx.load(std::memory_order_relaxed)) {
+    if (on) nvtxRangePushA(name);
+  }
+  ~NvtxScope() {
+    if (on) nvtxRangePop();
+  }
+};
 
 // ------------------------------ validation -------------------------------- //
 constexpr size_t ALIGN = 256;
@@ -189,6 +209,7 @@ struct FwdScratch {
   int32_t *ids, *slot, *row_of, *src_token, *counts, *offsets;
   float* gates;
   void *x_perm, *h, *y_perm;
+  float* row_gate;  // gate of each row (inference forward with the combine in the down product)
 };
 struct BwdScratch {
   void *dy_perm, *da, *db, *dx_perm;
@@ -220,6 +241,7 @@ FwdScratch carve_fwd(Carver& c, const Shape& s) {
   f.x_perm = c.take(R * s.d * es);
   f.h = c.take(R * s.f * es);
   f.y_perm = c.take(R * s.d * es);
+  f.row_gate = static_cast<float*>(c.take(R * 4));
   return f;
 }
 BwdScratch carve_bwd(Carver& c, const Shape& s) {
@@ -481,6 +503,7 @@ moe_status moe_layer_fwd(const moe_config* cfg, const moe_weights* w, const void
   if (ws == nullptr || ws_bytes < need_ws) return MOE_ERR_WORKSPACE;
   uint32_t* err = nullptr;
   MOE_TRY(device_ready(&err));
+  NvtxScope range("moe_layer_fwd");
   Carver c(align_ws(ws));
   RoutingScratch rs = carve_routing(c, s);
   FwdScratch f;
@@ -497,6 +520,7 @@ moe_status moe_layer_fwd(const moe_config* cfg, const moe_weights* w, const void
     f.x_perm = saved->x_perm;
     f.h = saved->h;
     f.y_perm = saved->y_perm;
+    f.row_gate = nullptr;
     a = saved->a;
     b = saved->b;
     probs = saved->probs;
@@ -510,10 +534,20 @@ moe_status moe_layer_fwd(const moe_config* cfg, const moe_weights* w, const void
   MOE_TRY(do_router(s, x, w->W_r, w->bias, f.ids, f.gates, probs, f.slot, f.row_of, f.src_token, f.counts, f.offsets,
                     rs, err, stream));
   if (s.T == 0) return MOE_OK;
-  CUDA_TRY(launch_permute(s, x, f.row_of, f.counts, f.offsets, f.x_perm, err, stream));
+  // Inference forward of a bf16 layer with k <= 2: the combine runs in the down
+  // product's epilogue (y zeroed by the permute, each row added in once with
+  // its gate), so y_perm is neither written nor read back.
+  const bool fused = saved == nullptr && s.bf16 && s.k <= 2;
+  CUDA_TRY(launch_permute(s, x, f.row_of, f.counts, f.offsets, f.x_perm, err, stream, fused ? f.gates : nullptr,
+                          fused ? f.row_gate : nullptr, fused ? y : nullptr));
   FfnFwdArgs fa{f.x_perm, f.counts, f.offsets, w->W1, w->W3, w->W2, f.h, f.y_perm, a, b};
+  if (fused) {
+    fa.src_token = f.src_token;
+    fa.row_gate = f.row_gate;
+    fa.y_comb = y;
+  }
   MOE_TRY(do_ffn_fwd(s, fa, err, stream));
-  CUDA_TRY(launch_combine(s, f.y_perm, f.row_of, f.gates, y, err, stream));
+  if (!fused) CUDA_TRY(launch_combine(s, f.y_perm, f.row_of, f.gates, y, err, stream));
   return MOE_OK;
 }
 
@@ -631,6 +665,7 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* w, const void
   if (ws == nullptr || ws_bytes < ws_bytes_for(s, recompute ? 2 : 1)) return MOE_ERR_WORKSPACE;
   uint32_t* err = nullptr;
   MOE_TRY(device_ready(&err));
+  NvtxScope range("moe_layer_bwd");
   Carver c(align_ws(ws));
   carve_routing(c, s);
   BwdScratch bs = carve_bwd(c, s);
@@ -685,6 +720,11 @@ moe_status moe_profiler_enable(int on) {
     g_prof_recs.clear();
   }
   g_prof_on = on != 0;
+  return MOE_OK;
+}
+
+moe_status moe_nvtx_enable(int on) {
+  g_nvtx.store(on != 0, std::memory_order_relaxed);
   return MOE_OK;
 }
 

@@ -15,8 +15,12 @@
 // r-th of cs equal K ranges (cs = 1, 2, 4 or 8, the largest that keeps tiles x
 // cs within the SM count, so that few tokens still spread over the GPU): warp
 // 0 lane 0 loads 128x64 x tiles and the three E_pad x 64 weight tiles with
-// TMA, warp 1 lane 0 issues tcgen05.mma (M=128, N=E_pad, K=16) into an fp32
-// TMEM accumulator, and warps 2-5 read one token row per thread from TMEM.
+// TMA (the parts land as consecutive E_pad-row blocks: one K-major operand of
+// 3 * E_pad rows), warp 1 lane 0 issues one tcgen05.mma (M=128, N=3*E_pad,
+// K=16; 256 + 128 columns when E_pad = 128) per K step into an fp32 TMEM
+// accumulator of three column groups (x hi, x mid, x lo), and warps 2-5 read
+// one token row per thread from TMEM, adding each logit's three groups, lo +
+// mid first.
 // CTAs r > 0 park their partial logits in their shared memory; the first CTA
 // adds them over distributed shared memory in rank order (so the sum does not
 // depend on timing) and does softmax and top-k in registers (value
@@ -32,7 +36,7 @@ namespace moe {
 namespace {
 
 constexpr int RT = 128;  // tokens per tile
-constexpr int RK = 64;   // K per stage (128-byte rows)
+constexpr int RK = 64;   // columns of one box (128-byte rows)
 constexpr int HIST_TOK = 64;
 constexpr int R_THREADS = 192;
 constexpr int R_MAXK = 8;
@@ -40,20 +44,32 @@ constexpr int MAX_CS = 8;  // K ranges (cluster size) per token tile
 
 template <int N>
 struct RCfg {
-  // stages: up to N = 32 two CTAs fit on an SM (shared memory and registers),
-  // so a large T runs in one wave
-  static constexpr int NST = N <= 16 ? 5 : (N <= 32 ? 3 : (N <= 64 ? 4 : 3));
+  // up to N = 32 two CTAs fit on an SM (shared memory and registers), so a
+  // large T runs in one wave; the stages fill what is left of the CTA's share
   static constexpr int MIN_BLOCKS = N <= 32 ? 2 : 1;
-  static constexpr int A_BYTES = RT * RK * 2;
-  static constexpr int B_BYTES = 3 * N * RK * 2;
+  // boxes per stage: a stage reads RB * 128 contiguous bytes of each token row
+  static constexpr int RB = 1;
+  static constexpr int A_BYTES = RB * RT * RK * 2;
+  static constexpr int B_BYTES = RB * 3 * N * RK * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int STATIC_SMEM = 2 * R_MAXK * N * 4 + N * 4;
+  static constexpr int BUDGET = (MIN_BLOCKS == 2 ? 115712 : 232448) - STATIC_SMEM - 256 - 1024;
+  static constexpr int NST = BUDGET / STAGE > 8 ? 8 : BUDGET / STAGE;
   static constexpr int CTRL_OFF = NST * STAGE;
   static constexpr int SMEM = CTRL_OFF + 256 + 1024;
-  static constexpr uint32_t TCOLS = N < 32 ? 32 : N;
+  // accumulator columns: the three parts side by side
+  static constexpr int NS = 3 * N;
+  static constexpr uint32_t TCOLS = NS <= 64 ? 64 : (NS <= 128 ? 128 : (NS <= 256 ? 256 : 512));
+  static_assert(NST >= 2, "at least two stages");
   static_assert(RT * (N + 4) * 4 <= NST * STAGE, "partial logits fit in the stage buffers");
-  // fp32 D, bf16 A and B, both K-major, M = 128, N
-  static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
-                                    ((uint32_t)(RT >> 4) << 24);
+  // MMA widths: one of 3 * E_pad columns, or 256 + 128 for E_pad = 128
+  static constexpr int N0 = NS <= 256 ? NS : 256;
+  static constexpr int N1 = NS - N0;
+  // fp32 D, bf16 A and B, both K-major, M = 128, N = N0 or N1
+  static constexpr uint32_t IDESC0 = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N0 >> 3) << 17) |
+                                     ((uint32_t)(RT >> 4) << 24);
+  static constexpr uint32_t IDESC1 = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)((N1 > 0 ? N1 : 16) >> 3) << 17) |
+                                     ((uint32_t)(RT >> 4) << 24);
 };
 
 struct RouterTcArgs {
@@ -219,7 +235,7 @@ __global__ void __launch_bounds__(R_THREADS, RCfg<N>::MIN_BLOCKS) router_tc_kern
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const uint32_t smem_base = smem_addr(smem);
-  const int kall = a.d / RK;
+  const int kall = a.d / (RK * C::RB);
   const int kb0 = (int)rank * kall / (int)cs, kb1 = ((int)rank + 1) * kall / (int)cs;
   const int kblocks = kb1 - kb0;
   // Tiles start their K loop at different k-blocks, so CTAs running together
@@ -246,9 +262,13 @@ __global__ void __launch_bounds__(R_THREADS, RCfg<N>::MIN_BLOCKS) router_tc_kern
         const uint32_t fb = smem_addr(&full_bar[stage]);
         mbar_expect_tx(fb, C::STAGE);
         const uint32_t sA = smem_base + stage * C::STAGE;
-        tma_load_2d(sA, &map_x, fb, (kb0 + kb) * RK, tile * RT);
 #pragma unroll
-        for (int s = 0; s < 3; ++s) tma_load_2d(sA + C::A_BYTES + s * N * 128, &map_w, fb, (kb0 + kb) * RK, s * N);
+        for (int b = 0; b < C::RB; ++b) {
+          const int col = ((kb0 + kb) * C::RB + b) * RK;
+          tma_load_2d(sA + b * RT * 128, &map_x, fb, col, tile * RT);
+#pragma unroll
+          for (int s = 0; s < 3; ++s) tma_load_2d(sA + C::A_BYTES + (b * 3 + s) * N * 128, &map_w, fb, col, s * N);
+        }
         ++issued;
         if (++stage == C::NST) {
           stage = 0;
@@ -283,13 +303,16 @@ __global__ void __launch_bounds__(R_THREADS, RCfg<N>::MIN_BLOCKS) router_tc_kern
         const uint32_t sA = smem_base + stage * C::STAGE;
         const uint32_t sB = sA + C::A_BYTES;
 #pragma unroll
-        for (int k16 = 0; k16 < RK / 16; ++k16) {
-          const uint64_t ad = sdesc(sA + k16 * 32, 16, 1024);
+        for (int b = 0; b < C::RB; ++b)
 #pragma unroll
-          for (int s = 0; s < 3; ++s)
-            umma_bf16(tmem_base, ad, sdesc(sB + s * N * 128 + k16 * 32, 16, 1024), C::IDESC,
-                      (i | k16 | s) != 0 ? 1u : 0u);
-        }
+          for (int k16 = 0; k16 < RK / 16; ++k16) {
+            const uint64_t ad = sdesc(sA + b * RT * 128 + k16 * 32, 16, 1024);
+            const uint32_t acc = (i | b | k16) != 0 ? 1u : 0u;
+            const uint32_t sBb = sB + b * 3 * N * 128;
+            umma_bf16(tmem_base, ad, sdesc(sBb + k16 * 32, 16, 1024), C::IDESC0, acc);
+            if (C::N1 > 0)
+              umma_bf16(tmem_base + C::N0, ad, sdesc(sBb + C::N0 * 128 + k16 * 32, 16, 1024), C::IDESC1, acc);
+          }
         umma_commit(smem_addr(&empty_bar[stage]));
         if (++stage == C::NST) {
           stage = 0;
@@ -308,11 +331,17 @@ __global__ void __launch_bounds__(R_THREADS, RCfg<N>::MIN_BLOCKS) router_tc_kern
       tc_fence_after();
 #pragma unroll
       for (int c = 0; c < N / 16; ++c) {
-        uint32_t r[16];
-        tmem_ld16(tmem_base + ((uint32_t)(q * 32) << 16) + c * 16, r);
-        tmem_ld_wait16(r);
+        uint32_t hi[16], mid[16], lo[16];
+        const uint32_t col = tmem_base + ((uint32_t)(q * 32) << 16) + c * 16;
+        tmem_ld16(col, hi);
+        tmem_ld16(col + N, mid);
+        tmem_ld16(col + 2 * N, lo);
+        tmem_ld_wait16(hi);
+        tmem_reg_fence16(mid);
+        tmem_reg_fence16(lo);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[c * 16 + i] = __uint_as_float(r[i]);
+        for (int i = 0; i < 16; ++i)
+          v[c * 16 + i] = (__uint_as_float(lo[i]) + __uint_as_float(mid[i])) + __uint_as_float(hi[i]);
       }
       have = true;
       if (rank != 0) {
@@ -451,7 +480,7 @@ int sm_count() {
 
 }  // namespace
 
-bool router_tc_supported(const Shape& s) { return s.bf16 && s.T >= RT && s.d % RK == 0 && s.E <= 128; }
+bool router_tc_supported(const Shape& s) { return s.bf16 && s.T >= RT && s.d % 256 == 0 && s.E <= 128; }
 
 size_t router_wsplit_bytes(const Shape& s) { return (size_t)3 * padded_experts(s.E) * s.d * 2; }
 
@@ -476,7 +505,8 @@ cudaError_t launch_router_tc(const Shape& s, const void* x, const float* W_r, co
   // K ranges per tile: the most (up to 8) that keep one CTA per SM and at
   // least two k-blocks per range
   int cs = 1;
-  while (cs < MAX_CS && tiles * cs * 2 <= sm_count() && s.d / RK >= 4 * cs) cs *= 2;
+  const int rb = N == 16 ? RCfg<16>::RB : (N == 32 ? RCfg<32>::RB : (N == 64 ? RCfg<64>::RB : RCfg<128>::RB));
+  while (cs < MAX_CS && tiles * cs * 2 <= sm_count() && s.d / (RK * rb) >= 4 * cs) cs *= 2;
   switch (N) {
     case 16: return launch_n<16>(mx, mw, a, tiles, cs, st);
     case 32: return launch_n<32>(mx, mw, a, tiles, cs, st);

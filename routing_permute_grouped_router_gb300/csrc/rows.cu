@@ -55,6 +55,8 @@ __device__ __forceinline__ void zero_pad_rows(const int32_t* counts, const int32
 // -------------------------------------------------------------------------- //
 // Permute (scatter form: each token row is read once and written to each of
 // its kept rows); blocks past the token range zero the pad rows of one expert.
+// When the combine is fused into the down product it also zeroes the token's
+// row of y and records the gate of each kept row.
 // -------------------------------------------------------------------------- //
 struct PermArgs {
   const char* x;
@@ -62,6 +64,9 @@ struct PermArgs {
   const int32_t* counts;
   const int32_t* offsets;
   char* x_perm;
+  const float* gates;  // with row_gate and y_zero: the fused combine's inputs
+  float* row_gate;
+  char* y_zero;
   uint32_t* err;
   int T, E, nvec;  // nvec = 16-byte vectors per row
   int64_t max_rows;
@@ -81,6 +86,15 @@ __global__ void __launch_bounds__(RW_WARPS * 32) permute_kernel(PermArgs a) {
   if (t >= a.T) return;
   int64_t rows[K];
   load_rows<K>(a.row_of, t, a.max_rows, a.err, lane, 10, rows);
+  if (a.row_gate != nullptr) {
+    if (lane < K) {
+#pragma unroll
+      for (int j = 0; j < K; ++j)
+        if (lane == j && rows[j] >= 0) a.row_gate[rows[j]] = a.gates[(size_t)t * K + j];
+    }
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    for (int v = lane; v < a.nvec; v += 32) stg16(a.y_zero + ((int64_t)t * a.nvec + v) * 16, z);
+  }
   const char* __restrict__ src = a.x + (int64_t)t * a.nvec * 16;
   char* __restrict__ dst = a.x_perm;
   for (int v0 = 0; v0 < a.nvec; v0 += 32 * INFLIGHT) {
@@ -521,9 +535,10 @@ struct PermuteL {  // byte copies: the element type does not matter
 }  // namespace
 
 cudaError_t launch_permute(const Shape& s, const void* x, const int32_t* row_of, const int32_t* counts,
-                           const int32_t* offsets, void* x_perm, uint32_t* err, cudaStream_t st) {
-  PermArgs a{static_cast<const char*>(x), row_of, counts, offsets, static_cast<char*>(x_perm), err,
-             s.T, s.E, row_vecs(s), s.max_rows, (s.T + RW_WARPS - 1) / RW_WARPS};
+                           const int32_t* offsets, void* x_perm, uint32_t* err, cudaStream_t st, const float* gates,
+                           float* row_gate, void* y_zero) {
+  PermArgs a{static_cast<const char*>(x), row_of, counts, offsets, static_cast<char*>(x_perm), gates, row_gate,
+             static_cast<char*>(y_zero), err, s.T, s.E, row_vecs(s), s.max_rows, (s.T + RW_WARPS - 1) / RW_WARPS};
   LaunchScope ls(KK_PERMUTE, st);
   return launch_typed_k<PermuteL>(s, a, a.token_blocks + s.E, st);
 }

@@ -176,6 +176,9 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 __device__ __forceinline__ void tmem_ld_wait16(uint32_t (&r)[16]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" : TMEM_REGS16(r)::"memory");
 }
+// Ties registers of a tcgen05.ld issued before an earlier tmem_ld_wait16 to
+// that wait, so no use of them is scheduled ahead of it.
+__device__ __forceinline__ void tmem_reg_fence16(uint32_t (&r)[16]) { asm volatile("" : TMEM_REGS16(r)::"memory"); }
 
 }  // namespace
 }  // namespace moe

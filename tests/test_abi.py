@@ -127,3 +127,11 @@ def test_recompute_workspace_is_larger_and_training_flag_checked(lib):
     assert w2 - w1 >= 3 * R * 512 * 2  # a, b, h of the recompute
     with pytest.raises(pkg.MoeError):
         pkg.moe_workspace_size(cfg, 3)
+
+
+def test_nvtx_switch_is_host_only(lib):
+    # toggling the NVTX ranges touches no device: it works without a GPU
+    n0 = lib.moe_launch_count()
+    assert lib.moe_nvtx_enable(1) == 0
+    assert lib.moe_nvtx_enable(0) == 0
+    assert lib.moe_launch_count() == n0

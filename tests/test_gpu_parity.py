@@ -219,6 +219,48 @@ def test_huge_capacity_equals_dropless_bitwise():
     assert torch.equal(outs[0], outs[1])
 
 
+@pytest.mark.parametrize("shape", [SMALL["top2_e8_small"], SMALL["zipf_e64_small"],
+                                   LS("inf_k1_drop", 900, 256, 512, 6, 1, 0.8, W.BF16)])
+def test_inference_forward_is_bit_identical_run_to_run(shape):
+    """The inference forward of a bf16 layer with k <= 2 adds each kept row into
+    y from the down product's epilogue; with at most two additions onto a zeroed
+    element the order in which they land cannot change y, so repeated runs are
+    bit for bit equal, and y matches the oracle."""
+    wl = W.make(shape, seed=13, micro_batches=1, with_dy=False)
+    L = layer.from_workload(wl, training=False)
+    x = wl.x[0].torch("cuda")
+    outs = []
+    for _ in range(3):
+        L.y.fill_(7.0)  # anything the forward leaves unwritten would show
+        outs.append(L.forward(x)[: shape.T].clone())
+    torch.cuda.synchronize()
+    check_no_device_error()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    assert_close("y", outs[0], _oracle_fwd(wl)["y"], TOL[shape.dtype])
+
+
+def test_nvtx_ranges_change_nothing():
+    """With NVTX ranges on around every launch and layer call the step runs as
+    without them, bit for bit."""
+    s = SMALL["top2_e8_small"]
+    wl = W.make(s, seed=3, micro_batches=1, with_dy=True)
+    res = []
+    for on in (False, True):
+        pkg.moe_nvtx_enable(on)
+        try:
+            L = layer.from_workload(wl)
+            x = wl.x[0].torch("cuda")
+            L.forward(x)
+            L.backward(x, wl.dy[0].torch("cuda"), accumulate=False)
+            torch.cuda.synchronize()
+        finally:
+            pkg.moe_nvtx_enable(False)
+        check_no_device_error()
+        res.append([L.y.clone(), L.dx.clone(), L.grads["dW1"].clone(), L.grads["dW_r"].clone()])
+    for u, v in zip(*res):
+        assert torch.equal(u, v)
+
+
 def test_runs_are_bit_identical():
     s = SMALL["train_e16_small"]
     wl = W.make(s, micro_batches=1, with_dy=True)
