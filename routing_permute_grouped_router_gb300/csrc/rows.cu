@@ -325,23 +325,109 @@ __global__ void __launch_bounds__(RW_WARPS * 32) dx_router_kernel(DxArgs a) {
   pdl_enter();  // see pdl_wait: no global access before this
   constexpr int VN = Vec<Tx>::N;
   constexpr int U = INFLIGHT / K > 0 ? INFLIGHT / K : 1;
+  constexpr int US = INFLIGHT / (2 * K) > 0 ? INFLIGHT / (2 * K) : 1;  // sparse path: half, as W_r rows load too
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int t = blockIdx.x * RW_WARPS + warp;
   if (t >= a.T) return;
   int64_t rows[K];
   load_rows<K>(a.row_of, t, a.max_rows, a.err, lane, 13, rows);
-  // Experts with a nonzero logit gradient (at most k of them when k > 1),
-  // found with all lanes active before the row loop.
+  // Experts with a nonzero logit gradient, found with all lanes active before
+  // the row loop.
   const float* dlt = a.dl + (size_t)t * a.E;
   unsigned nzmask[4];
+  float dlv[4];
+  int nnz = 0;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const int e = 32 * c + lane;
-    const float mine = (e < a.E) ? dlt[e] : 0.f;
-    nzmask[c] = __ballot_sync(0xffffffffu, mine != 0.f);
+    dlv[c] = (e < a.E) ? dlt[e] : 0.f;
+    nzmask[c] = __ballot_sync(0xffffffffu, dlv[c] != 0.f);
+    nnz += __popc(nzmask[c]);
   }
   const char* __restrict__ xp = a.dx_perm;
   char* __restrict__ dst = a.dx + (int64_t)t * a.nvec * 16;
+  if (nnz <= K) {
+    // Sparse logit gradient (at most k nonzero experts: k > 1 without an extra
+    // term): the experts and their dl values in expert order, so that their
+    // W_r^T rows are loaded together with the dx_perm rows.
+    int ez[K];
+    float wz[K];
+    unsigned m0 = nzmask[0], m1 = nzmask[1], m2 = nzmask[2], m3 = nzmask[3];
+#pragma unroll
+    for (int n = 0; n < K; ++n) {
+      unsigned mm = m0;
+      int cb = 0;
+      float sv = dlv[0];
+      if (m0 == 0u) {
+        mm = m1; cb = 32; sv = dlv[1];
+        if (m1 == 0u) {
+          mm = m2; cb = 64; sv = dlv[2];
+          if (m2 == 0u) { mm = m3; cb = 96; sv = dlv[3]; }
+        }
+      }
+      const int src = mm ? __ffs(mm) - 1 : 0;
+      const float w = __shfl_sync(0xffffffffu, sv, src);
+      ez[n] = mm ? cb + src : -1;
+      wz[n] = mm ? w : 0.f;
+      if (m0) m0 &= m0 - 1;
+      else if (m1) m1 &= m1 - 1;
+      else if (m2) m2 &= m2 - 1;
+      else if (m3) m3 &= m3 - 1;
+    }
+    for (int v0 = 0; v0 < a.nvec; v0 += 32 * US) {
+      uint4 buf[K][US];
+      float4 wv[K][US][VN / 4];
+#pragma unroll
+      for (int j = 0; j < K; ++j)
+#pragma unroll
+        for (int u = 0; u < US; ++u) {
+          const int v = v0 + lane + 32 * u;
+          buf[j][u] = (rows[j] >= 0 && v < a.nvec) ? ldg16(xp + (rows[j] * a.nvec + v) * 16) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+      for (int n = 0; n < K; ++n)
+#pragma unroll
+        for (int u = 0; u < US; ++u) {
+          const int v = v0 + lane + 32 * u;
+          const float4* wr = reinterpret_cast<const float4*>(a.W_rT + (size_t)(ez[n] >= 0 ? ez[n] : 0) * a.d +
+                                                             (size_t)v * VN);
+#pragma unroll
+          for (int qq = 0; qq < VN / 4; ++qq)
+            wv[n][u][qq] = (ez[n] >= 0 && v < a.nvec) ? __ldg(wr + qq) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+      for (int u = 0; u < US; ++u) {
+        const int v = v0 + lane + 32 * u;
+        if (v >= a.nvec) continue;
+        float acc[VN];
+#pragma unroll
+        for (int i = 0; i < VN; ++i) acc[i] = 0.f;
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+          if (rows[j] < 0) continue;
+          float val[VN];
+          unpack(buf[j][u], val);
+#pragma unroll
+          for (int i = 0; i < VN; ++i) acc[i] += val[i];
+        }
+#pragma unroll
+        for (int n = 0; n < K; ++n) {
+          const float w = wz[n];  // 0 for missing experts: adds exact zeros, as the loop below skips them
+          if (ez[n] < 0) continue;
+#pragma unroll
+          for (int qq = 0; qq < VN / 4; ++qq) {
+            acc[4 * qq + 0] = fmaf(w, wv[n][u][qq].x, acc[4 * qq + 0]);
+            acc[4 * qq + 1] = fmaf(w, wv[n][u][qq].y, acc[4 * qq + 1]);
+            acc[4 * qq + 2] = fmaf(w, wv[n][u][qq].z, acc[4 * qq + 2]);
+            acc[4 * qq + 3] = fmaf(w, wv[n][u][qq].w, acc[4 * qq + 3]);
+          }
+        }
+        stg16(dst + v * 16, pack(acc));
+      }
+    }
+    return;
+  }
+  // dense logit gradient (k = 1, or an added term): every nonzero expert in turn
   for (int v0 = 0; v0 < a.nvec; v0 += 32 * U) {
     uint4 buf[K][U];
 #pragma unroll
