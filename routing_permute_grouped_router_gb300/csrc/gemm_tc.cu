@@ -60,15 +60,14 @@ constexpr uint32_t TMEM_COLS = 256 * ACC_BUFS;
 constexpr int MAX_E = 128;
 constexpr int MAX_SMEM = 232448;  // 227 KB per CTA
 constexpr int MAX_ST = 6;
-constexpr int WG_AHEAD = 2;  // wgrad: old-gradient boxes requested ahead of the one being added
-// wgrad: tiles of odd rounds (tile index / pairs) walk their K rows backwards.
-// Every tile of an expert streams the same row range; when one round's tiles
-// end and the next round's begin at different times, the new tiles start
-// where the last of the old ones still read, so the rows they share stay in
-// L2.  The direction is a function of the tile index, not of timing.
-constexpr bool WG_SERPENTINE = false;
 
-enum Mode { M_UP = 0, M_DOWN = 1, M_DGRAD_H = 2, M_DGRAD_X = 3, M_WGRAD = 4, M_DOWN_COMB = 5 };
+enum Mode { M_UP = 0, M_DOWN = 1, M_DGRAD_H = 2, M_DGRAD_X = 3, M_WGRAD = 4, M_DOWN_COMB = 5, M_WGRAD_L = 6 };
+// wgrad comes in two shapes, chosen on the host from the expert capacity:
+// M_WGRAD for short K per tile (capacity-limited layers: the fp32 gradient
+// read-modify-write dominates, so four staged gradient boxes a warp with two
+// in flight, and five 32 KB stages) and M_WGRAD_L for long K (dropless
+// layers: three 64 KB stages of two k-blocks, two gradient boxes a warp).
+__host__ __device__ constexpr bool is_wgrad(int m) { return m == M_WGRAD || m == M_WGRAD_L; }
 
 // Pipeline depth and epilogue staging per product.  Each epilogue warp owns two
 // output boxes (double buffering of its TMA stores).  dgrad h also stages its a
@@ -83,11 +82,17 @@ static_assert(320 + (3 * 128 + 2) * 4 <= 2048, "control block");
 constexpr int KB_NARROW = 2;  // 64-wide k-blocks per stage of the products with light epilogues
 template <int MODE>
 struct ModeCfg {
-  static constexpr bool WIDE = MODE == M_DGRAD_H || MODE == M_WGRAD;  // four staged boxes per warp
-  static constexpr int KB = WIDE ? 1 : KB_NARROW;  // k-blocks of 64 behind one pair of barriers
-  static constexpr int NST = (WIDE ? 5 : 6) / KB;
+  // k-blocks of 64 behind one pair of barriers
+  static constexpr int KB = (MODE == M_DGRAD_H || MODE == M_WGRAD) ? 1 : KB_NARROW;
+  // wgrad: staged fp32 gradient boxes per epilogue warp, and old-gradient boxes
+  // requested ahead of the one being added
+  static constexpr int WBUFS = MODE == M_WGRAD ? 4 : 2;
+  static constexpr int WAHEAD = MODE == M_WGRAD ? 2 : 1;
   static constexpr int STAGE = KB * STAGE_BYTES;
-  static constexpr int EPI_WARP_BYTES = (WIDE ? 4 : 2) * BOX_BYTES;
+  static constexpr int EPI_WARP_BYTES = (MODE == M_DGRAD_H ? 4 : (is_wgrad(MODE) ? WBUFS : 2)) * BOX_BYTES;
+  // as many stages as fit next to the epilogue staging, at most MAX_ST
+  static constexpr int NST0 = (MAX_SMEM - CTRL_BYTES - 1024 - EPI_WARPS * EPI_WARP_BYTES) / STAGE;
+  static constexpr int NST = NST0 > MAX_ST ? MAX_ST : NST0;
   static constexpr int EPI_OFF = NST * STAGE;
   static constexpr int CTRL_OFF = EPI_OFF + EPI_WARPS * EPI_WARP_BYTES;
   static constexpr int SMEM = CTRL_OFF + CTRL_BYTES + 1024;  // + alignment slack
@@ -95,6 +100,7 @@ struct ModeCfg {
 static_assert(ModeCfg<M_UP>::SMEM <= MAX_SMEM, "shared memory budget");
 static_assert(ModeCfg<M_DGRAD_H>::SMEM <= MAX_SMEM, "shared memory budget");
 static_assert(ModeCfg<M_WGRAD>::SMEM <= MAX_SMEM, "shared memory budget");
+static_assert(ModeCfg<M_WGRAD_L>::SMEM <= MAX_SMEM && ModeCfg<M_WGRAD_L>::NST >= 3, "shared memory budget");
 
 // Tensor maps per product (loads of the mainloop first, then epilogue maps):
 //   UP      0 x_perm, 1 W1, 2 W3, 3 h (store), 4 a (store), 5 b (store)
@@ -191,7 +197,6 @@ struct Tile {
   int64_t row0;  // ragged-M modes: this CTA's first row; WGRAD: first K row
   int m0, n0;    // WGRAD: this CTA's output rows m0.. and the tile's columns n0..; others: n0
   int sub;       // WGRAD product: 0 = dW1, 1 = dW3, 2 = dW2
-  bool kback;    // WGRAD: K rows visited from the last k-block to the first
   int kblocks;
   bool valid;    // this CTA's rows belong to the tile's expert
 };
@@ -216,7 +221,7 @@ __device__ __forceinline__ int n_tiles_of(const TcArgs& a) {
 // expert's rows, which share L2.
 template <int MODE>
 __device__ __forceinline__ int sched_tile(int j, int pair, int npairs, int total, bool interleave) {
-  if (MODE != M_WGRAD || !interleave) {
+  if (!is_wgrad(MODE) || !interleave) {
     const int tile = pair + j * npairs;
     return tile < total ? tile : -1;
   }
@@ -233,7 +238,7 @@ __device__ __forceinline__ Tile decode(int tile, uint32_t rank, const TcArgs& a,
                                        const int* s_pair) {
   Tile t{};
   t.valid = true;
-  if (MODE == M_WGRAD) {
+  if (is_wgrad(MODE)) {
     const int P = (a.d / (2 * BM)) * (a.f / BN);  // pair tiles of one product of one expert
     t.e = s_pair[tile / (3 * P)];
     const int q = tile % (3 * P);
@@ -250,8 +255,9 @@ __device__ __forceinline__ Tile decode(int tile, uint32_t rank, const TcArgs& a,
     t.m0 = (r / nt) * 2 * BM + (int)rank * BM;
     t.n0 = (r % nt) * BN;
     t.row0 = s_off[t.e];
-    t.kblocks = (s_cnt[t.e] + BK - 1) / BK;
-    t.kback = WG_SERPENTINE && ((tile / (int)(gridDim.x / 2)) & 1);
+    // stages of KB k-blocks; the segment is 128-row aligned and zero past its
+    // rows, so a last stage reaching past the rows reads zeros of the segment
+    t.kblocks = (s_cnt[t.e] + BK * ModeCfg<MODE>::KB - 1) / (BK * ModeCfg<MODE>::KB);
   } else {
     // expert e owns tiles [s_pair[e] * nt, s_pair[e + 1] * nt); inside it the
     // column blocks run fastest, so the CTAs working at one time share a few
@@ -317,7 +323,7 @@ __device__ __forceinline__ void issue_stage(const TcMaps& maps, const TcArgs& a,
   } else {  // WGRAD
     const CUtensorMap* am = t.sub == 2 ? &maps.m[1] : &maps.m[0];
     const CUtensorMap* bm = t.sub == 0 ? &maps.m[2] : (t.sub == 1 ? &maps.m[3] : &maps.m[4]);
-    const int kr = r0 + (t.kback ? t.kblocks - 1 - kb : kb) * BK;
+    const int kr = r0 + kb * BK;
     ld(sA, am, t.m0, kr);
     ld(sA + 8192, am, t.m0 + 64, kr);
     ld(sB, bm, t.n0 + nh, kr);
@@ -377,17 +383,23 @@ __device__ __forceinline__ bool epilogue_tile(const TcMaps& maps, const TcArgs& 
   }
   // wgrad accumulating into the fp32 gradient: fetch the first box of old
   // values while the mainloop still runs (read, add and store back below)
-  const bool wg_add = MODE == M_WGRAD && a.accumulate && t.kblocks > 0;
-  const int wg_rows = MODE == M_WGRAD ? (t.sub == 2 ? a.f : a.d) : 0;
-  const CUtensorMap* wg_map = &maps.m[MODE == M_WGRAD ? 5 + t.sub : 0];
+  constexpr int WG_BUFS = ModeCfg<MODE>::WBUFS, WG_AHEAD = ModeCfg<MODE>::WAHEAD;
+  const bool wg_add = is_wgrad(MODE) && a.accumulate && t.kblocks > 0;
+  const int wg_rows = is_wgrad(MODE) ? (t.sub == 2 ? a.f : a.d) : 0;
+  const CUtensorMap* wg_map = &maps.m[is_wgrad(MODE) ? 5 + t.sub : 0];
   const int wg_orow = t.e * wg_rows + t.m0 + q * 32;
   if (wg_add) {
     // boxes 0 and 1 of the tile: their buffers were last read by the stores of
     // boxes nbox-4 and nbox-3, older than the two latest stores
-    if (lane == 0) bulk_wait_read2();
+    // their buffers were last read by the stores of boxes nbox + c - WG_BUFS,
+    // older than the WG_BUFS - WG_AHEAD latest stores
+    if (lane == 0) {
+      if (WG_BUFS - WG_AHEAD >= 2) bulk_wait_read2();
+      else bulk_wait_read1();
+    }
 #pragma unroll
     for (int c = 0; c < WG_AHEAD; ++c) {
-      const uint32_t h = (es.nbox + c) & 3u;
+      const uint32_t h = (es.nbox + c) % WG_BUFS;
       if (lane == 0) {
         const uint32_t bar = lbar + 8 * h;
         mbar_expect_tx(bar, BOX_BYTES);
@@ -534,16 +546,20 @@ __device__ __forceinline__ bool epilogue_tile(const TcMaps& maps, const TcArgs& 
     }
     es.nbox += 4;
   } else if (wg_add) {  // WGRAD, accumulate: dW += acc via TMA load, add, TMA store
-    // four buffers per warp; the old values of box c + 2 are requested while
-    // box c is added, so two loads are in flight behind the one being used
+    // WG_BUFS buffers per warp; the old values of box c + WG_AHEAD are
+    // requested while box c is added, so WG_AHEAD loads are in flight behind
+    // the one being used
 #pragma unroll 1
     for (int c = 0; c < 8; ++c) {
       const uint32_t g = es.nbox + c;
-      const uint32_t h = g & 3u;
+      const uint32_t h = g % WG_BUFS;
       if (c + WG_AHEAD < 8) {
-        const uint32_t hn = (g + WG_AHEAD) & 3u;
+        const uint32_t hn = (g + WG_AHEAD) % WG_BUFS;
         if (lane == 0) {
-          bulk_wait_read1();  // every store but the latest (box c - 1) has read its buffer
+          // buffer hn was last read by the store of box c + WG_AHEAD - WG_BUFS:
+          // at most WG_BUFS - WG_AHEAD - 1 newer stores may still be reading
+          if (WG_BUFS - WG_AHEAD - 1 >= 1) bulk_wait_read1();
+          else bulk_wait_read0();
           const uint32_t bar = lbar + 8 * hn;
           mbar_expect_tx(bar, BOX_BYTES);
           tma_load_2d(ebuf + hn * BOX_BYTES, wg_map, bar, t.n0 + (c + WG_AHEAD) * 32, wg_orow);
@@ -635,7 +651,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
   for (int i = threadIdx.x; i <= a.E; i += THREADS) s_off[i] = a.offsets[i];
   for (int i = threadIdx.x; i < a.E; i += THREADS) s_cnt[i] = a.counts[i];
   __syncthreads();
-  if (MODE == M_WGRAD) {
+  if (is_wgrad(MODE)) {
     // experts ordered by rows, most first (the rank of each expert, computed in parallel)
     for (int e = threadIdx.x; e < a.E; e += THREADS) {
       int r = 0;
@@ -667,7 +683,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
     int total = 0;
     *s_interleave = 0;
     if (ok && same_tmem) {
-      if (MODE == M_WGRAD) {
+      if (is_wgrad(MODE)) {
         total = a.E * 3 * (a.d / (2 * BM)) * (a.f / BN);
         // interleave long and short tiles only when some tiles are long (at least
         // 64 k-blocks) and the experts' rows differ at least eightfold
@@ -695,7 +711,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer (both CTAs) ----------------
-      constexpr int NLOAD = MODE == M_UP ? 3 : (MODE == M_DGRAD_X ? 4 : (MODE == M_WGRAD ? 5 : 2));
+      constexpr int NLOAD = MODE == M_UP ? 3 : (MODE == M_DGRAD_X ? 4 : (is_wgrad(MODE) ? 5 : 2));
       for (int i = 0; i < NLOAD; ++i) prefetch_map(&maps.m[i]);
       int stage = 0;
       uint32_t phase = 0;
@@ -751,8 +767,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       // ---------------- MMA issuer (first CTA of the pair) ----------------
-      constexpr bool A_MN = MODE == M_WGRAD;
-      constexpr bool B_MN = MODE == M_UP || MODE == M_DOWN || MODE == M_DOWN_COMB || MODE == M_WGRAD;
+      constexpr bool A_MN = is_wgrad(MODE);
+      constexpr bool B_MN = MODE == M_UP || MODE == M_DOWN || MODE == M_DOWN_COMB || is_wgrad(MODE);
       constexpr uint32_t IDESC = idesc_bf16(A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
@@ -1024,7 +1040,12 @@ cudaError_t tc_ffn_bwd(const Shape& s, const FfnBwdArgs& b, uint32_t* err, cudaS
   a.w0 = b.dW1;
   a.w1 = b.dW3;
   a.w2 = b.dW2;
-  e = launch_mode<M_WGRAD>(mw, a, (int64_t)s.E * 3 * (s.d / (2 * BM)) * (s.f / BN), KK_GEMM_WGRAD, st);
+  // long K per tile (dropless, or a capacity above 2048 rows): the wide-stage shape
+  const int64_t wg_tiles = (int64_t)s.E * 3 * (s.d / (2 * BM)) * (s.f / BN);
+  if (s.cap > 2048)
+    e = launch_mode<M_WGRAD_L>(mw, a, wg_tiles, KK_GEMM_WGRAD, st);
+  else
+    e = launch_mode<M_WGRAD>(mw, a, wg_tiles, KK_GEMM_WGRAD, st);
   if (e != cudaSuccess) return e;
   a.o0 = static_cast<__nv_bfloat16*>(b.dx_perm);
   a.o1 = nullptr;
