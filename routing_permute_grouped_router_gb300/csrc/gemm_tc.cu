@@ -61,13 +61,19 @@ constexpr int MAX_E = 128;
 constexpr int MAX_SMEM = 232448;  // 227 KB per CTA
 constexpr int MAX_ST = 6;
 
-enum Mode { M_UP = 0, M_DOWN = 1, M_DGRAD_H = 2, M_DGRAD_X = 3, M_WGRAD = 4, M_DOWN_COMB = 5, M_WGRAD_L = 6 };
+enum Mode { M_UP = 0, M_DOWN = 1, M_DGRAD_H = 2, M_DGRAD_X = 3, M_WGRAD = 4, M_DOWN_COMB = 5, M_WGRAD_L = 6,
+            M_DGRAD_H_L = 7 };
 // wgrad comes in two shapes, chosen on the host from the expert capacity:
 // M_WGRAD for short K per tile (capacity-limited layers: the fp32 gradient
 // read-modify-write dominates, so four staged gradient boxes a warp with two
 // in flight, and five 32 KB stages) and M_WGRAD_L for long K (dropless
 // layers: three 64 KB stages of two k-blocks, two gradient boxes a warp).
 __host__ __device__ constexpr bool is_wgrad(int m) { return m == M_WGRAD || m == M_WGRAD_L; }
+// dgrad h likewise: M_DGRAD_H (five 32 KB stages, its a|b boxes double-buffered)
+// for short K, M_DGRAD_H_L for d >= 4096 (three 64 KB stages of two k-blocks,
+// one a|b buffer a warp: a chunk's a and b are requested once the previous
+// chunk's da and db have left the buffer, behind a long mainloop).
+__host__ __device__ constexpr bool is_dgrad_h(int m) { return m == M_DGRAD_H || m == M_DGRAD_H_L; }
 
 // Pipeline depth and epilogue staging per product.  Each epilogue warp owns two
 // output boxes (double buffering of its TMA stores).  dgrad h also stages its a
@@ -89,7 +95,9 @@ struct ModeCfg {
   static constexpr int WBUFS = MODE == M_WGRAD ? 4 : 2;
   static constexpr int WAHEAD = MODE == M_WGRAD ? 2 : 1;
   static constexpr int STAGE = KB * STAGE_BYTES;
-  static constexpr int EPI_WARP_BYTES = (MODE == M_DGRAD_H ? 4 : (is_wgrad(MODE) ? WBUFS : 2)) * BOX_BYTES;
+  static constexpr int ABUFS = MODE == M_DGRAD_H ? 2 : 1;  // dgrad h: [a | b] box pairs per warp
+  static constexpr int EPI_WARP_BYTES =
+      (is_dgrad_h(MODE) ? 2 * ABUFS : (is_wgrad(MODE) ? WBUFS : 2)) * BOX_BYTES;
   // as many stages as fit next to the epilogue staging, at most MAX_ST
   static constexpr int NST0 = (MAX_SMEM - CTRL_BYTES - 1024 - EPI_WARPS * EPI_WARP_BYTES) / STAGE;
   static constexpr int NST = NST0 > MAX_ST ? MAX_ST : NST0;
@@ -99,6 +107,7 @@ struct ModeCfg {
 };
 static_assert(ModeCfg<M_UP>::SMEM <= MAX_SMEM, "shared memory budget");
 static_assert(ModeCfg<M_DGRAD_H>::SMEM <= MAX_SMEM, "shared memory budget");
+static_assert(ModeCfg<M_DGRAD_H_L>::SMEM <= MAX_SMEM && ModeCfg<M_DGRAD_H_L>::NST >= 3, "shared memory budget");
 static_assert(ModeCfg<M_WGRAD>::SMEM <= MAX_SMEM, "shared memory budget");
 static_assert(ModeCfg<M_WGRAD_L>::SMEM <= MAX_SMEM && ModeCfg<M_WGRAD_L>::NST >= 3, "shared memory budget");
 
@@ -205,7 +214,7 @@ template <int MODE>
 __device__ __forceinline__ int n_tiles_of(const TcArgs& a) {
   if (MODE == M_UP) return a.f / 128;
   if (MODE == M_DOWN || MODE == M_DOWN_COMB || MODE == M_DGRAD_X) return a.d / BN;
-  return a.f / BN;  // DGRAD_H
+  return a.f / BN;  // DGRAD_H, DGRAD_H_L
 }
 
 // The j-th tile of pair `pair`, or -1 past the last one.  Tiles are dealt
@@ -279,7 +288,7 @@ __device__ __forceinline__ Tile decode(int tile, uint32_t rank, const TcArgs& a,
     const int local = 2 * (l / nt) + (int)rank;
     t.valid = local < (s_off[t.e + 1] - s_off[t.e]) / BM;
     t.row0 = (int64_t)s_off[t.e] + (int64_t)local * BM;
-    const int K = (MODE == M_UP || MODE == M_DGRAD_H) ? a.d : ((MODE == M_DOWN || MODE == M_DOWN_COMB) ? a.f : 2 * a.f);
+    const int K = (MODE == M_UP || is_dgrad_h(MODE)) ? a.d : ((MODE == M_DOWN || MODE == M_DOWN_COMB) ? a.f : 2 * a.f);
     t.kblocks = K / (BK * ModeCfg<MODE>::KB);
   }
   return t;
@@ -308,7 +317,7 @@ __device__ __forceinline__ void issue_stage(const TcMaps& maps, const TcArgs& a,
     const int wr = t.e * a.f + kb * BK;
     ld(sB, &maps.m[1], t.n0 + nh, wr);
     ld(sB + 8192, &maps.m[1], t.n0 + nh + 64, wr);
-  } else if (MODE == M_DGRAD_H) {
+  } else if (is_dgrad_h(MODE)) {
     ld(sA, &maps.m[0], kb * BK, r0);
     ld(sB, &maps.m[1], kb * BK, t.e * a.f + t.n0 + nh);
   } else if (MODE == M_DGRAD_X) {
@@ -368,9 +377,9 @@ __device__ __forceinline__ bool epilogue_tile(const TcMaps& maps, const TcArgs& 
     return true;
   }
   const int row0 = static_cast<int>(t.row0) + q * 32;
-  if (MODE == M_DGRAD_H) {
+  if (is_dgrad_h(MODE)) {
     // fetch the first a/b boxes of the tile while its mainloop still runs
-    const uint32_t h = es.nbox & 1;
+    const uint32_t h = ModeCfg<MODE>::ABUFS == 2 ? (es.nbox & 1) : 0;
     if (lane == 0) {
       bulk_wait_read0();
       const uint32_t bar = lbar + 8 * h;
@@ -497,12 +506,13 @@ __device__ __forceinline__ bool epilogue_tile(const TcMaps& maps, const TcArgs& 
       box_issue_store(om, buf, t.n0 + c * 64, row0, lane);
       ++es.nbox;
     }
-  } else if (MODE == M_DGRAD_H) {
+  } else if (is_dgrad_h(MODE)) {
+    constexpr bool DOUBLE = ModeCfg<MODE>::ABUFS == 2;
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
-      const uint32_t h = (es.nbox + c) & 1;
+      const uint32_t h = DOUBLE ? ((es.nbox + c) & 1) : 0u;
       const uint32_t buf = ebuf + h * 2 * BOX_BYTES;  // [a box | b box], overwritten with [da | db]
-      if (c + 1 < 4) {
+      if (DOUBLE && c + 1 < 4) {
         const uint32_t hn = h ^ 1u;
         if (lane == 0) {
           bulk_wait_read0();  // the stores that last used buffer hn have read it
@@ -542,6 +552,17 @@ __device__ __forceinline__ bool epilogue_tile(const TcMaps& maps, const TcArgs& 
         tma_store_2d(&maps.m[4], buf, t.n0 + c * 64, row0);
         tma_store_2d(&maps.m[5], buf + BOX_BYTES, t.n0 + c * 64, row0);
         bulk_commit();
+      }
+      if (!DOUBLE && c + 1 < 4) {
+        // one buffer: the next chunk's a and b once da and db have been read out
+        if (lane == 0) {
+          bulk_wait_read0();
+          mbar_expect_tx(lbar, 2 * BOX_BYTES);
+          tma_load_2d(buf, &maps.m[2], lbar, t.n0 + (c + 1) * 64, row0);
+          tma_load_2d(buf + BOX_BYTES, &maps.m[3], lbar, t.n0 + (c + 1) * 64, row0);
+        }
+        es.pending[0] = true;
+        __syncwarp();
       }
     }
     es.nbox += 4;
@@ -1035,7 +1056,9 @@ cudaError_t tc_ffn_bwd(const Shape& s, const FfnBwdArgs& b, uint32_t* err, cudaS
   a.o1 = static_cast<__nv_bfloat16*>(b.db);
   a.i0 = static_cast<const __nv_bfloat16*>(b.a);
   a.i1 = static_cast<const __nv_bfloat16*>(b.b);
-  cudaError_t e = launch_mode<M_DGRAD_H>(mh, a, mp * (s.f / BN), KK_GEMM_DGRAD_H, st);
+  // long K (d >= 4096): the wide-stage shape
+  cudaError_t e = s.d >= 4096 ? launch_mode<M_DGRAD_H_L>(mh, a, mp * (s.f / BN), KK_GEMM_DGRAD_H, st)
+                              : launch_mode<M_DGRAD_H>(mh, a, mp * (s.f / BN), KK_GEMM_DGRAD_H, st);
   if (e != cudaSuccess) return e;
   a.w0 = b.dW1;
   a.w1 = b.dW3;

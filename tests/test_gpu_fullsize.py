@@ -102,6 +102,34 @@ def test_dropless_e32_routing_full_and_sampled_outputs():
     assert_close("y[sampled]", L.y[torch.from_numpy(toks).cuda()], ref, TOL)
 
 
+def test_dropless_e32_full_backward_sampled():
+    """The largest layer's backward at full size, twice accumulated: dx on sampled
+    tokens and dW1, dW3, dW2 on sampled columns against the oracle (the long-K
+    wgrad and dgrad h shapes run here)."""
+    s = W.WORKLOADS["dropless_e32_bf16"]
+    wl = W.make(s, micro_batches=1, with_dy=True)
+    L = layer.from_workload(wl)
+    x, dy = wl.x[0].torch("cuda"), wl.dy[0].torch("cuda")
+    L.forward(x)
+    L.backward(x, dy, accumulate=False)
+    L.backward(x, dy, accumulate=True)
+    torch.cuda.synchronize()
+    check_no_device_error()
+    xs, dys = wl.x[0].f32, wl.dy[0].f32
+    W1, W3, W2 = wl.W1.f32, wl.W3.f32, wl.W2.f32
+    st = O.route(xs, wl.W_r, wl.bias, s.k, None)
+    assert_routing_equal(L.saved, st, s.T)
+    toks = _sample(s.T, 96, 3)
+    outs = [O.token_outputs(t, xs, dys, wl.W_r, wl.bias, W1, W3, W2, st) for t in toks]
+    assert_close("dx[sampled]", L.dx[torch.from_numpy(toks).cuda()], np.stack([o["dx"] for o in outs]), TOL)
+    cols = _sample(s.d_ff, 24, 4)
+    c = O.weight_grad_columns(xs, dys, W1, W3, W2, st, cols)
+    ci = torch.from_numpy(cols).cuda()
+    assert_close("dW1[:, :, cols]", L.grads["dW1"][:, :, ci], 2 * c["dW1"], TOL)
+    assert_close("dW3[:, :, cols]", L.grads["dW3"][:, :, ci], 2 * c["dW3"], TOL)
+    assert_close("dW2[:, cols, :]", L.grads["dW2"][:, ci, :], 2 * c["dW2"], TOL)
+
+
 def test_train_e16_four_micro_batches_sampled():
     s = W.WORKLOADS["train_e16_bf16"]
     wl = W.make(s)
