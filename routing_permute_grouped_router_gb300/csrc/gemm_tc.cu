@@ -137,6 +137,9 @@ struct TcArgs {
   const int32_t* src_token;  // DOWN_COMBINE: token of each row (-1: pad row)
   const float* row_gate;     // DOWN_COMBINE: gate of each row
   __nv_bfloat16* y;          // DOWN_COMBINE: [T, d] output, zeroed beforehand
+  const float* rdl;          // DGRAD_X, optional: logit gradient dl [T, E]; with it the row's
+  const float* rwr;          //   router term dl[token, e] * W_r[:, e] is added (W_r [d, E])
+  int rE;
   int accumulate;
   uint32_t* err;
 };
@@ -418,6 +421,20 @@ __device__ __forceinline__ bool epilogue_tile(const TcMaps& maps, const TcArgs& 
     }
     __syncwarp();
   }
+  // dgrad x with the router term of the kept rows: each lane's row gets
+  // dl[token, e] * W_r[columns, e] added before rounding (e = the tile's expert);
+  // the token's dl and the tile's W_r values are fetched while the mainloop runs
+  const bool rfuse = MODE == M_DGRAD_X && a.rdl != nullptr;
+  float rg = 0.f;
+  float rw[8];
+#pragma unroll
+  for (int sl = 0; sl < 8; ++sl) rw[sl] = 0.f;
+  if (rfuse) {
+    const int tok = a.src_token[(int64_t)row0 + lane];
+    rg = tok >= 0 ? a.rdl[(int64_t)tok * a.rE + t.e] : 0.f;
+#pragma unroll
+    for (int sl = 0; sl < 8; ++sl) rw[sl] = a.rwr[(int64_t)(t.n0 + sl * 32 + lane) * a.rE + t.e];
+  }
   if (!mbar_wait(tfull, tfull_parity, abort_flag, a.err, 400 + MODE)) return false;
   tc_fence_after();
 
@@ -490,17 +507,21 @@ __device__ __forceinline__ bool epilogue_tile(const TcMaps& maps, const TcArgs& 
     }
   } else if (MODE == M_DOWN || MODE == M_DGRAD_X) {
     const CUtensorMap* om = MODE == M_DOWN ? &maps.m[2] : &maps.m[4];
-#pragma unroll 1
+#pragma unroll
     for (int c = 0; c < 4; ++c) {
       const uint32_t buf = ebuf + (es.nbox & 1) * BOX_BYTES;
       stage_wait(lane);
-#pragma unroll 1
+#pragma unroll
       for (int s = 0; s < 2; ++s) {
         uint32_t r[32];
         tmem_ld32(tacc + c * 64 + s * 32, r);
         tmem_ld_wait(r);
         float v[32];
         regs_to_f32(r, v);
+        if (rfuse) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = fmaf(rg, __shfl_sync(0xffffffffu, rw[c * 2 + s], i), v[i]);
+        }
         box_put_bf16x32(buf, lane, 4 * s, v);
       }
       box_issue_store(om, buf, t.n0 + c * 64, row0, lane);
@@ -1072,6 +1093,10 @@ cudaError_t tc_ffn_bwd(const Shape& s, const FfnBwdArgs& b, uint32_t* err, cudaS
   if (e != cudaSuccess) return e;
   a.o0 = static_cast<__nv_bfloat16*>(b.dx_perm);
   a.o1 = nullptr;
+  a.rdl = b.rdl;
+  a.rwr = b.rwr;
+  a.rE = s.E;
+  a.src_token = b.src_token;
   return launch_mode<M_DGRAD_X>(mx, a, mp * (s.d / BN), KK_GEMM_DGRAD_X, st);
 }
 

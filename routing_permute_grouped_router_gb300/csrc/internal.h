@@ -94,8 +94,11 @@ cudaError_t launch_combine_bwd(const Shape& s, const void* dy, const void* y_per
                                const int32_t* row_of, const float* gates, const float* probs,
                                const int32_t* counts, const int32_t* offsets, void* dy_perm, float* dg, float* dl,
                                uint32_t* err, cudaStream_t st);
+// With ids given (skip_kept), the router terms of the token's kept experts are
+// taken to be in dx_perm already and only the other experts' terms are added.
 cudaError_t launch_dx_router(const Shape& s, const void* dx_perm, const int32_t* row_of, const float* dl,
-                             const float* W_r, float* W_rT, void* dx, uint32_t* err, cudaStream_t st);
+                             const float* W_r, float* W_rT, void* dx, uint32_t* err, cudaStream_t st,
+                             const int32_t* ids = nullptr);
 cudaError_t launch_dwr(const Shape& s, const void* x, const float* dl, float* partial, float* dW_r, int accumulate,
                        cudaStream_t st);
 int dwr_splits(const Shape& s);  // token slices of the router-weight gradient (partial buffer [splits][d][E])
@@ -132,6 +135,9 @@ struct FfnBwdArgs {
   const void* W1; const void* W3; const void* W2;
   void* da; void* db; void* dx_perm;
   float* dW1; float* dW3; float* dW2; int accumulate;
+  // bf16 only, optional: with rdl (dl [T, E]), rwr (W_r [d, E]) and src_token
+  // set, dx_perm[row] also holds the row's router term dl[token, e] * W_r[:, e]
+  const float* rdl = nullptr; const float* rwr = nullptr; const int32_t* src_token = nullptr;
 };
 cudaError_t tc_ffn_fwd(const Shape& s, const FfnFwdArgs& a, uint32_t* err, cudaStream_t st);
 cudaError_t tc_ffn_bwd(const Shape& s, const FfnBwdArgs& a, uint32_t* err, cudaStream_t st);

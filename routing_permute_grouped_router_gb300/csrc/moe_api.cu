@@ -326,12 +326,12 @@ moe_status do_ffn_bwd(const Shape& s, const FfnBwdArgs& b, uint32_t* err, cudaSt
 
 moe_status do_dx_router(const Shape& s, const void* x, const void* dx_perm, const int32_t* row_of, const float* dl,
                         const float* W_r, void* dx, float* dW_r, int accumulate, const BwdScratch& bs, uint32_t* err,
-                        cudaStream_t st) {
+                        cudaStream_t st, const int32_t* kept_ids = nullptr) {
   if (s.T == 0) {
     if (!accumulate) CUDA_TRY(cudaMemsetAsync(dW_r, 0, (size_t)s.d * s.E * 4, st));
     return MOE_OK;
   }
-  CUDA_TRY(launch_dx_router(s, dx_perm, row_of, dl, W_r, bs.W_rT, dx, err, st));
+  CUDA_TRY(launch_dx_router(s, dx_perm, row_of, dl, W_r, bs.W_rT, dx, err, st, kept_ids));
   if (dwr_tc_supported(s)) {
     CUDA_TRY(launch_dwr_tc(s, x, dl, bs.dlsplit, bs.partial, err, st));
     CUDA_TRY(launch_dwr_reduce(bs.partial, dW_r, dwr_tc_ranges(s), (int64_t)s.d * s.E, accumulate, st));
@@ -654,7 +654,7 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* w, const void
     MOE_TRY(need(saved->b));
     MOE_TRY(need(saved->h));
   }
-  const void* sp4[] = {saved->ids, saved->gates, saved->row_of, saved->counts, saved->offsets};
+  const void* sp4[] = {saved->ids, saved->gates, saved->row_of, saved->src_token, saved->counts, saved->offsets};
   for (const void* p : sp4) MOE_TRY(need(p, 4));
   if (s.k == 1 || s.aux > 0.f) MOE_TRY(need(saved->probs, 4));
   if (grads->aux_loss != nullptr) MOE_TRY(need(grads->aux_loss, 4));
@@ -686,8 +686,18 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* w, const void
   CUDA_TRY(launch_aux_loss(s, s.aux, saved->probs, saved->ids, grads->aux_loss, bs.dl, bs.aux, err, stream));
   FfnBwdArgs fb{saved->x_perm, act_a, act_b, act_h, bs.dy_perm, saved->counts, saved->offsets,
                 w->W1, w->W3, w->W2, bs.da, bs.db, bs.dx_perm, grads->dW1, grads->dW3, grads->dW2, accumulate};
+  // bf16 layers: the router term of each kept row, dl[t, e] W_r[:, e], is added
+  // in the dgrad x epilogue (its expert is the tile's), so the dx gather adds
+  // only the terms of the experts a token does not keep a row for
+  const bool fuse_router = s.bf16 != 0;
+  if (fuse_router) {
+    fb.rdl = bs.dl;
+    fb.rwr = w->W_r;
+    fb.src_token = saved->src_token;
+  }
   MOE_TRY(do_ffn_bwd(s, fb, err, stream));
-  return do_dx_router(s, x, bs.dx_perm, saved->row_of, bs.dl, w->W_r, dx, grads->dW_r, accumulate, bs, err, stream);
+  return do_dx_router(s, x, bs.dx_perm, saved->row_of, bs.dl, w->W_r, dx, grads->dW_r, accumulate, bs, err, stream,
+                      fuse_router ? saved->ids : nullptr);
 }
 
 moe_status moe_get_device_error(int32_t* code, int32_t* detail, int clear) {

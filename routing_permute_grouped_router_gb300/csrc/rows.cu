@@ -312,6 +312,7 @@ __global__ void transpose_wr_kernel(const float* W_r, float* W_rT, int d, int E)
 struct DxArgs {
   const char* dx_perm;
   const int32_t* row_of;
+  const int32_t* ids;  // non-null: the kept experts' router terms are already in dx_perm
   const float* dl;
   const float* W_rT;
   char* dx;
@@ -325,7 +326,7 @@ __global__ void __launch_bounds__(RW_WARPS * 32) dx_router_kernel(DxArgs a) {
   pdl_enter();  // see pdl_wait: no global access before this
   constexpr int VN = Vec<Tx>::N;
   constexpr int U = INFLIGHT / K > 0 ? INFLIGHT / K : 1;
-  constexpr int US = INFLIGHT / (2 * K) > 0 ? INFLIGHT / (2 * K) : 1;  // sparse path: half, as W_r rows load too
+  constexpr int US = U;  // sparse path: the W_r^T vectors load alongside the rows' (no spills up to k = 8)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int t = blockIdx.x * RW_WARPS + warp;
   if (t >= a.T) return;
@@ -334,6 +335,9 @@ __global__ void __launch_bounds__(RW_WARPS * 32) dx_router_kernel(DxArgs a) {
   // Experts with a nonzero logit gradient, found with all lanes active before
   // the row loop.
   const float* dlt = a.dl + (size_t)t * a.E;
+  int kept[K];  // experts whose router term dx_perm already holds (or -1)
+#pragma unroll
+  for (int j = 0; j < K; ++j) kept[j] = (a.ids != nullptr && rows[j] >= 0) ? a.ids[(size_t)t * K + j] : -1;
   unsigned nzmask[4];
   float dlv[4];
   int nnz = 0;
@@ -341,11 +345,46 @@ __global__ void __launch_bounds__(RW_WARPS * 32) dx_router_kernel(DxArgs a) {
   for (int c = 0; c < 4; ++c) {
     const int e = 32 * c + lane;
     dlv[c] = (e < a.E) ? dlt[e] : 0.f;
+#pragma unroll
+    for (int j = 0; j < K; ++j)
+      if (e == kept[j]) dlv[c] = 0.f;
     nzmask[c] = __ballot_sync(0xffffffffu, dlv[c] != 0.f);
     nnz += __popc(nzmask[c]);
   }
   const char* __restrict__ xp = a.dx_perm;
   char* __restrict__ dst = a.dx + (int64_t)t * a.nvec * 16;
+  if (nnz == 0) {
+    // no router term left to add (all in dx_perm already, or dl zero): the k
+    // rows' sum alone, with U vectors of every row in flight
+    for (int v0 = 0; v0 < a.nvec; v0 += 32 * U) {
+      uint4 buf[K][U];
+#pragma unroll
+      for (int j = 0; j < K; ++j)
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int v = v0 + lane + 32 * u;
+          buf[j][u] = (rows[j] >= 0 && v < a.nvec) ? ldg16(xp + (rows[j] * a.nvec + v) * 16) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + lane + 32 * u;
+        if (v >= a.nvec) continue;
+        float acc[VN];
+#pragma unroll
+        for (int i = 0; i < VN; ++i) acc[i] = 0.f;
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+          if (rows[j] < 0) continue;
+          float val[VN];
+          unpack(buf[j][u], val);
+#pragma unroll
+          for (int i = 0; i < VN; ++i) acc[i] += val[i];
+        }
+        stg16(dst + v * 16, pack(acc));
+      }
+    }
+    return;
+  }
   if (nnz <= K) {
     // Sparse logit gradient (at most k nonzero experts: k > 1 without an extra
     // term): the experts and their dl values in expert order, so that their
@@ -458,7 +497,7 @@ __global__ void __launch_bounds__(RW_WARPS * 32) dx_router_kernel(DxArgs a) {
         while (nz) {
           const int e = 32 * c + __ffs(nz) - 1;
           nz &= nz - 1;
-          const float w = dlt[e];
+          const float w = dlt[e];  // e is not a kept expert here (those were masked before the ballot)
           const float4* wr = reinterpret_cast<const float4*>(a.W_rT + (size_t)e * a.d + (size_t)v * VN);
 #pragma unroll
           for (int qq = 0; qq < VN / 4; ++qq) {
@@ -650,7 +689,8 @@ cudaError_t launch_combine_bwd(const Shape& s, const void* dy, const void* y_per
 }
 
 cudaError_t launch_dx_router(const Shape& s, const void* dx_perm, const int32_t* row_of, const float* dl,
-                             const float* W_r, float* W_rT, void* dx, uint32_t* err, cudaStream_t st) {
+                             const float* W_r, float* W_rT, void* dx, uint32_t* err, cudaStream_t st,
+                             const int32_t* ids) {
   if (s.T == 0) return cudaSuccess;
   {
     dim3 grid((s.d + 31) / 32, (s.E + 31) / 32);
@@ -658,7 +698,7 @@ cudaError_t launch_dx_router(const Shape& s, const void* dx_perm, const int32_t*
     cudaError_t e = launch_pdl(transpose_wr_kernel, grid, dim3(32, 8), 0, st, W_r, W_rT, s.d, s.E);
     if (e != cudaSuccess) return e;
   }
-  DxArgs a{static_cast<const char*>(dx_perm), row_of, dl, W_rT, static_cast<char*>(dx), err, s.T, s.E, s.d,
+  DxArgs a{static_cast<const char*>(dx_perm), row_of, ids, dl, W_rT, static_cast<char*>(dx), err, s.T, s.E, s.d,
            row_vecs(s), s.max_rows};
   LaunchScope ls(KK_DX_ROUTER, st);
   return launch_typed_k<DxL>(s, a, (s.T + RW_WARPS - 1) / RW_WARPS, st);
