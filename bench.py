@@ -431,8 +431,10 @@ def run_ours(args, world, rank, local):
         # copy and step i-1's result copy run while step i computes, as a
         # training loop that feeds the layer would.  Each tensor moves as
         # N_COPY row chunks on N_COPY copy streams per direction, so several
-        # copy engines share the host link.
-        N_COPY = 4
+        # copy engines share the host link; below 64 MB a direction one copy
+        # per tensor (the extra launches and events would cost more than the
+        # copies they overlap).
+        N_COPY = 4 if (x.numel() + dy.numel()) * x.element_size() >= (64 << 20) else 1
         hx = x.cpu().pin_memory()
         hdy = dy.cpu().pin_memory()
         hy = torch.empty_like(L.y, device="cpu").pin_memory()
@@ -500,8 +502,9 @@ def run_ours(args, world, rank, local):
         e2e = {"value": world * s.T * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": (x.numel() + dy.numel()) * es,
                "d2h_bytes_per_step": (L.y.numel() + L.dx.numel()) * es,
-               "note": "pinned host x, dy -> device and y, dx -> pinned host every step, four copy streams "
-                       "each way overlapping the neighbouring steps' compute; forward + backward; no L2 flush"}
+               "note": f"pinned host x, dy -> device and y, dx -> pinned host every step, {N_COPY} copy "
+                       f"stream{'s' if N_COPY > 1 else ''} each way overlapping the neighbouring steps' "
+                       "compute; forward + backward; no L2 flush"}
 
     if rank != 0:
         return

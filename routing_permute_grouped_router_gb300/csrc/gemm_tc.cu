@@ -94,6 +94,11 @@ struct ModeCfg {
   // requested ahead of the one being added
   static constexpr int WBUFS = MODE == M_WGRAD ? 4 : 2;
   static constexpr int WAHEAD = MODE == M_WGRAD ? 2 : 1;
+  // wgrad with interleaved tiles: stages of the long (host) tile issued
+  // between two short (guest) tiles, about 8 us of MMA work, longer than one
+  // guest's epilogue; and the most stages a guest may have
+  static constexpr int GUEST_GAP = KB == 2 ? 12 : 24;
+  static constexpr int GUEST_MAX = KB == 2 ? 12 : 24;
   static constexpr int STAGE = KB * STAGE_BYTES;
   static constexpr int ABUFS = MODE == M_DGRAD_H ? 2 : 1;  // dgrad h: [a | b] box pairs per warp
   static constexpr int EPI_WARP_BYTES =
@@ -220,26 +225,78 @@ __device__ __forceinline__ int n_tiles_of(const TcArgs& a) {
   return a.f / BN;  // DGRAD_H, DGRAD_H_L
 }
 
-// The j-th tile of pair `pair`, or -1 past the last one.  Tiles are dealt
-// round-robin.  When WGRAD's experts differ widely in rows (`interleave`), it
-// lists its tiles by expert from the most rows to the fewest (s_pair holds
-// that expert order) and deals them from both ends of the list: the pair takes
-// two consecutive places of a round, and place m is the (m / 2)-th tile from
-// the front when m is even, from the back when odd.  Each pair so alternates a
-// long, tensor-bound tile with a short one whose fp32 gradient
-// read-modify-write is HBM-bound, and the short tile's epilogue runs under the
-// next long tile's mainloop instead of in a separate tail.  With experts of
-// similar size the plain order keeps the tiles running together on one
-// expert's rows, which share L2.
+// Work is dealt to the pairs in groups: one host tile and g >= 0 guest tiles.
+// Without interleaving every group is one tile, dealt round-robin (group j of
+// pair p is tile p + j * npairs) into the two TMEM accumulators in turn.
+//
+// When WGRAD's experts differ widely in rows (`interleave`), its tiles are
+// listed by expert from the most rows to the fewest (s_pair holds that expert
+// order).  A tile's fp32 gradient read-modify-write (its epilogue) takes about
+// as long whatever its K, so a short tile finishes its MMAs well before the
+// epilogue of the tile before it is done, and with two accumulators the next
+// MMA would wait for that epilogue.  So each round gives every pair one host
+// from the front of the list and, when the host is long, g guests from the
+// back: the pair issues GUEST_GAP stages of the host, one whole guest, the
+// next GUEST_GAP stages, the next guest, ... and the rest of the host.  The
+// host holds one accumulator for its whole K loop while the guests take turns
+// in the other, each guest's epilogue running under the next host stages.
+// Commits, and so epilogues, come in the order guest 0 .. guest g-1, host.
+// Group k puts its host in accumulator k & 1 and its guests in the other:
+// the next host then takes the accumulator the last guest used (its epilogue
+// comes before this host's), and the next guests the one this host used.
+// g is the same for all pairs of a round (from the round's last, shortest
+// host: one guest per GUEST_GAP stages, with at least GUEST_GAP stages of the
+// host after the last guest), and guests have at most GUEST_MAX stages.
+struct Group {
+  int host;   // tile index of the host
+  int g;      // guests
+  int gbase;  // guest i is tile gbase - i
+};
+struct GroupIter {
+  int F, B;  // interleaving: the tiles not yet dealt are [F, B)
+  int j;     // round-robin: the next group
+};
+
+// stages (of KB k-blocks) of WGRAD tile `tile`: its expert's rows over BK * KB
 template <int MODE>
-__device__ __forceinline__ int sched_tile(int j, int pair, int npairs, int total, bool interleave) {
+__device__ __forceinline__ int wg_stages(int tile, const TcArgs& a, const int* s_cnt, const int* s_pair) {
+  const int P = (a.d / (2 * BM)) * (a.f / BN);
+  const int c = s_cnt[s_pair[tile / (3 * P)]];
+  return (c + BK * ModeCfg<MODE>::KB - 1) / (BK * ModeCfg<MODE>::KB);
+}
+
+// The next group of pair `pair`; false past the last one.  Every role of
+// every CTA walks the same sequence of rounds, so they agree on the groups.
+template <int MODE>
+__device__ __forceinline__ bool next_group(GroupIter& it, Group& gr, int pair, int npairs, int total,
+                                           bool interleave, const TcArgs& a, const int* s_cnt,
+                                           const int* s_pair) {
+  gr.g = 0;
+  gr.gbase = 0;
   if (!is_wgrad(MODE) || !interleave) {
-    const int tile = pair + j * npairs;
-    return tile < total ? tile : -1;
+    gr.host = pair + it.j * npairs;
+    ++it.j;
+    return gr.host < total;
   }
-  const int m = (j >> 1) * 2 * npairs + 2 * pair + (j & 1);
-  if (m >= total) return -1;
-  return (m & 1) ? total - 1 - (m >> 1) : (m >> 1);
+  if (it.F >= it.B) return false;
+  const int left = it.B - it.F;
+  int g = 0;
+  if (left > npairs) {
+    // the round's last host is its shortest
+    g = wg_stages<MODE>(it.F + npairs - 1, a, s_cnt, s_pair) / ModeCfg<MODE>::GUEST_GAP - 1;
+    const int room = (left - npairs) / npairs;
+    if (g > room) g = room;
+    while (g > 0 && wg_stages<MODE>(it.B - g * npairs, a, s_cnt, s_pair) > ModeCfg<MODE>::GUEST_MAX) --g;
+    if (g < 0) g = 0;
+  }
+  const int F0 = it.F, B0 = it.B;
+  it.F += npairs;
+  it.B -= g * npairs;
+  if (pair >= (left < npairs ? left : npairs)) return false;
+  gr.host = F0 + pair;
+  gr.g = g;
+  gr.gbase = B0 - 1 - pair * g;
+  return true;
 }
 
 // s_pair[e]: pair tiles (of 2 x 128 rows) before expert e in the ragged-M modes;
@@ -759,26 +816,35 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
       uint32_t phase = 0;
       int issued = 0;
       bool alive = true;
-      int tile;
-      for (int j = 0; (tile = sched_tile<MODE>(j, pair, npairs, total, interleave)) >= 0 && alive; ++j) {
-        const Tile t = decode<MODE>(tile, rank, a, s_off, s_cnt, s_pair);
-        for (int kb = 0; kb < t.kblocks; ++kb) {
-          if (!mbar_wait(smem_addr(&empty_bar[stage]), phase ^ 1u, abort_flag, a.err, 100 + MODE)) {
-            alive = false;
-            break;
-          }
-          const uint32_t fb_local = smem_addr(&full_bar[stage]);
-          if (rank == 0) mbar_expect_tx(fb_local, Cfg::KB * PAIR_STAGE_BYTES);
-          const uint32_t fb = rank == 0 ? fb_local : mapa_shared(fb_local, 0);
+      // one stage of tile t: its k-blocks kb * KB .. kb * KB + KB - 1
+      auto load_stage = [&](const Tile& t, int kb) -> bool {
+        if (!mbar_wait(smem_addr(&empty_bar[stage]), phase ^ 1u, abort_flag, a.err, 100 + MODE)) return false;
+        const uint32_t fb_local = smem_addr(&full_bar[stage]);
+        if (rank == 0) mbar_expect_tx(fb_local, Cfg::KB * PAIR_STAGE_BYTES);
+        const uint32_t fb = rank == 0 ? fb_local : mapa_shared(fb_local, 0);
 #pragma unroll
-          for (int kk = 0; kk < Cfg::KB; ++kk) {
-            const uint32_t sA = smem_base + stage * Cfg::STAGE + kk * STAGE_BYTES;
-            issue_stage<MODE>(maps, a, t, kb * Cfg::KB + kk, sA, sA + A_BYTES, fb, rank);
-          }
-          ++issued;
-          if (++stage == NST) {
-            stage = 0;
-            phase ^= 1u;
+        for (int kk = 0; kk < Cfg::KB; ++kk) {
+          const uint32_t sA = smem_base + stage * Cfg::STAGE + kk * STAGE_BYTES;
+          issue_stage<MODE>(maps, a, t, kb * Cfg::KB + kk, sA, sA + A_BYTES, fb, rank);
+        }
+        ++issued;
+        if (++stage == NST) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        return true;
+      };
+      GroupIter it{0, total, 0};
+      Group gr;
+      while (alive && next_group<MODE>(it, gr, pair, npairs, total, interleave, a, s_cnt, s_pair)) {
+        const Tile th = decode<MODE>(gr.host, rank, a, s_off, s_cnt, s_pair);
+        int hk = 0;
+        for (int i = 0; i <= gr.g && alive; ++i) {
+          const int hend = i < gr.g && (i + 1) * Cfg::GUEST_GAP < th.kblocks ? (i + 1) * Cfg::GUEST_GAP : th.kblocks;
+          for (; hk < hend && alive; ++hk) alive = load_stage(th, hk);
+          if (i < gr.g && alive) {
+            const Tile tg = decode<MODE>(gr.gbase - i, rank, a, s_off, s_cnt, s_pair);
+            for (int kb = 0; kb < tg.kblocks && alive; ++kb) alive = load_stage(tg, kb);
           }
         }
       }
@@ -814,21 +880,20 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
       constexpr uint32_t IDESC = idesc_bf16(A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
-      int local = 0;
+      uint32_t par = 0u;  // bit acc: parity of the completed uses of accumulator acc
       bool alive = true;
-      int tile;
-      for (int j = 0; (tile = sched_tile<MODE>(j, pair, npairs, total, interleave)) >= 0 && alive; ++j, ++local) {
-        const Tile t = decode<MODE>(tile, rank, a, s_off, s_cnt, s_pair);
-        const int acc = local % ACC_BUFS;
-        const uint32_t use = (uint32_t)(local / ACC_BUFS) & 1u;
-        if (!mbar_wait(smem_addr(&tempty_bar[acc]), use ^ 1u, abort_flag, a.err, 200 + MODE)) break;
+      // wait until the epilogue has emptied accumulator acc
+      auto acquire = [&](int acc) -> bool {
+        if (!mbar_wait(smem_addr(&tempty_bar[acc]), ((par >> acc) & 1u) ^ 1u, abort_flag, a.err, 200 + MODE))
+          return false;
         tc_fence_after();
+        return true;
+      };
+      // the MMAs of stages kb0 .. kb1 - 1 of tile t into accumulator acc
+      auto mma_stages = [&](const Tile& t, int acc, int kb0, int kb1) -> bool {
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < t.kblocks; ++kb) {
-          if (!mbar_wait(smem_addr(&full_bar[stage]), phase, abort_flag, a.err, 300 + MODE)) {
-            alive = false;
-            break;
-          }
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(smem_addr(&full_bar[stage]), phase, abort_flag, a.err, 300 + MODE)) return false;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < Cfg::KB; ++kk) {
@@ -847,8 +912,31 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
             phase ^= 1u;
           }
         }
+        return true;
+      };
+      GroupIter it{0, total, 0};
+      Group gr;
+      for (int k = 0; alive && next_group<MODE>(it, gr, pair, npairs, total, interleave, a, s_cnt, s_pair); ++k) {
+        const int ha = k & 1, ga = ha ^ 1;
+        const Tile th = decode<MODE>(gr.host, rank, a, s_off, s_cnt, s_pair);
+        if (!acquire(ha)) break;
+        int hk = 0;
+        for (int i = 0; i <= gr.g && alive; ++i) {
+          const int hend = i < gr.g && (i + 1) * Cfg::GUEST_GAP < th.kblocks ? (i + 1) * Cfg::GUEST_GAP : th.kblocks;
+          alive = mma_stages(th, ha, hk, hend);
+          hk = hend;
+          if (i < gr.g && alive) {
+            const Tile tg = decode<MODE>(gr.gbase - i, rank, a, s_off, s_cnt, s_pair);
+            alive = acquire(ga) && mma_stages(tg, ga, 0, tg.kblocks);
+            if (alive) {
+              umma_commit_pair(smem_addr(&tfull_bar[ga]), 0x3);
+              par ^= 1u << ga;
+            }
+          }
+        }
         if (!alive) break;
-        umma_commit_pair(smem_addr(&tfull_bar[acc]), 0x3);
+        umma_commit_pair(smem_addr(&tfull_bar[ha]), 0x3);
+        par ^= 1u << ha;
       }
       // all MMAs of the pair complete (in both CTAs' TMEM) before TMEM is released
       if (total > 0) umma_commit_pair(smem_addr(drain_bar), 0x3);
@@ -864,16 +952,14 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
     const uint32_t ebuf = smem_base + Cfg::EPI_OFF + ew * Cfg::EPI_WARP_BYTES;
     const uint32_t lbar = smem_addr(&load_bar[4 * ew]);
     EpiState es{0u, {0u, 0u, 0u, 0u}, {false, false, false, false}};
-    int local = 0;
-    int tile;
-    for (int j = 0; (tile = sched_tile<MODE>(j, pair, npairs, total, interleave)) >= 0; ++j, ++local) {
-      const Tile t = decode<MODE>(tile, rank, a, s_off, s_cnt, s_pair);
-      const int acc = local % ACC_BUFS;
-      const uint32_t use = (uint32_t)(local / ACC_BUFS) & 1u;
+    uint32_t par = 0u;  // bit acc: parity of the completed uses of accumulator acc
+    // the epilogue of tile t from accumulator acc, which is then released to the MMA
+    auto drain = [&](const Tile& t, int acc) -> bool {
       const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-      if (!epilogue_tile<MODE>(maps, a, t, tacc, q, lane, ebuf, lbar, es, smem_addr(&tfull_bar[acc]), use,
-                               abort_flag))
-        break;
+      if (!epilogue_tile<MODE>(maps, a, t, tacc, q, lane, ebuf, lbar, es, smem_addr(&tfull_bar[acc]),
+                               (par >> acc) & 1u, abort_flag))
+        return false;
+      par ^= 1u << acc;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -881,6 +967,15 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
         if (rank == 0) mbar_arrive(te);
         else mbar_arrive_cluster(mapa_shared(te, 0));
       }
+      return true;
+    };
+    GroupIter it{0, total, 0};
+    Group gr;
+    bool ok = true;
+    for (int k = 0; ok && next_group<MODE>(it, gr, pair, npairs, total, interleave, a, s_cnt, s_pair); ++k) {
+      const int ha = k & 1, ga = ha ^ 1;
+      for (int i = 0; i < gr.g && ok; ++i) ok = drain(decode<MODE>(gr.gbase - i, rank, a, s_off, s_cnt, s_pair), ga);
+      if (ok) ok = drain(decode<MODE>(gr.host, rank, a, s_off, s_cnt, s_pair), ha);
     }
     // input loads still in flight (only after an abort), then every store
     for (int h = 0; h < 4; ++h)
