@@ -207,10 +207,10 @@ def source_digest(name: str) -> str:
     return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
 
 
-def committed_traffic(name: str, workload: str):
-    """DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum) from the committed
-    profile of this workload, profiles/traffic_<workload>.json, when it was taken on the current
-    source of the kernel; None otherwise."""
+def committed_profile(name: str, workload: str):
+    """The committed one-pass ncu record of kernel `name` on this workload
+    (profiles/traffic_<workload>.json: DRAM bytes per launch and ncu duration), when it
+    was taken on the current source of the kernel; None otherwise."""
     path = os.path.join(PROFILE_DIR, f"traffic_{workload}.json")
     if not os.path.exists(path):
         return None
@@ -220,7 +220,14 @@ def committed_traffic(name: str, workload: str):
         return None
     if not rec or rec.get("source_sha") != source_digest(name):
         return None
-    return float(rec["dram_bytes_per_launch"])
+    return rec
+
+
+def committed_traffic(name: str, workload: str):
+    """DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum) from the committed
+    profile of this workload, when it was taken on the current source of the kernel; None otherwise."""
+    rec = committed_profile(name, workload)
+    return None if rec is None else float(rec["dram_bytes_per_launch"])
 
 
 def peaks():
@@ -524,6 +531,16 @@ def run_ours(args, world, rank, local):
             entry["gbs"] = round(nb / (avg / 1e3) / 1e9, 1)
             entry["frac_of_hbm"] = round(nb / (avg / 1e3) / 1e9 / hbm, 3)
             entry["bound"] = binding(fl, nb, avg / 1e3, tflops, hbm)["bound"]
+            # the same work over the kernel's duration in the committed ncu launch list
+            # (serialised, no launch or event overhead), when taken on the current source
+            rec = committed_profile(name, args.workload)
+            if rec is not None and rec.get("ncu_time_us"):
+                t_ncu = rec["ncu_time_us"] / 1e6
+                entry["ncu_us"] = rec["ncu_time_us"]
+                entry["dram_bytes_ncu"] = rec["dram_bytes_per_launch"]
+                entry["frac_of_hbm_ncu"] = round(nb / t_ncu / 1e9 / hbm, 3)
+                if fl:
+                    entry["frac_of_bf16_peak_ncu"] = round(fl / t_ncu / 1e12 / tflops, 3)
         kernels[name] = entry
     fl, nb = work.get(dom, (0, 0))
     avg_s = prof_dom[dom][1] / prof_dom[dom][0] / 1e3
@@ -556,7 +573,10 @@ def run_ours(args, world, rank, local):
         "kernels": kernels,
         "kernels_note": "per-kernel CUDA events from an untimed pass of min(steps, 50) steps; the timed "
                         "region records events only around the roofline kernel; gbs = algorithmic bytes / "
-                        "event time (an effective rate: reads that hit L2 count as moved)",
+                        "event time (an effective rate: reads that hit L2 count as moved); *_ncu: the same "
+                        "work over the kernel's duration in the committed one-pass ncu launch list of this "
+                        "workload (no launch or event overhead), present only when that list was taken on "
+                        "the kernel's current source",
     }
     if e2e is not None:
         line["e2e"] = e2e

@@ -130,21 +130,25 @@ __device__ __forceinline__ void token_epilogue(const RouterTcArgs& a, float (&v)
   for (int j = 0; j < R_MAXK; ++j) {
     lj[j] = 0.f;
     ej[j] = 0;
-    if (j < a.k) {
-      float bv = -INFINITY;
-      int be = -1;
+  }
+  // one pick per pass, the passes not unrolled: eight unrolled copies of the
+  // scan made the kernel's code several times larger, and with E = 64 the
+  // epilogue took 8 us longer
+#pragma unroll 1
+  for (int j = 0; j < a.k; ++j) {
+    float bv = -INFINITY;
+    int be = -1;
 #pragma unroll
-      for (int e = 0; e < N; ++e)
-        if (!((taken[e >> 5] >> (e & 31)) & 1u) && (be < 0 || v[e] > bv)) {  // strict: lower index on ties
-          bv = v[e];
-          be = e;
-        }
+    for (int e = 0; e < N; ++e)
+      if (!((taken[e >> 5] >> (e & 31)) & 1u) && (be < 0 || v[e] > bv)) {  // strict: lower index on ties
+        bv = v[e];
+        be = e;
+      }
 #pragma unroll
-      for (int w = 0; w < NW; ++w)
-        if ((be >> 5) == w) taken[w] |= 1u << (be & 31);
-      lj[j] = bv;
-      ej[j] = be;
-    }
+    for (int w = 0; w < NW; ++w)
+      if ((be >> 5) == w) taken[w] |= 1u << (be & 31);
+    lj[j] = bv;
+    ej[j] = be;
   }
   const float mx = lj[0];
   // the exponentials first (independent, so they overlap), then their sum in
