@@ -130,6 +130,44 @@ def test_dropless_e32_full_backward_sampled():
     assert_close("dW2[:, cols, :]", L.grads["dW2"][:, ci, :], 2 * c["dW2"], TOL)
 
 
+def test_dropless_skewed_wgrad_host_and_guest_tiles_sampled():
+    """wgrad with interleaved host and guest tiles away from the benchmark shape.
+
+    Dropless top-4 over 32 log-Zipf(1.3) experts, T = 8192, d = 2048, f = 1024:
+    the busiest expert gets about 7,700 rows (60 stages of 128) and the idlest
+    a few dozen, so the tiles are listed by expert size and each of the 96
+    pair tiles per expert may host guests; the first rounds' hosts lie in the
+    two busiest experts and carry two to four guests each, and later rounds
+    straddle experts of different sizes.  dW on sampled columns of every expert
+    and dx on sampled tokens against the oracle, after two accumulated passes.
+    """
+    s = W.LayerShape("dropless_skewed", 8192, 2048, 1024, 32, 4, 0.0, W.BF16, zipf_s=1.3)
+    wl = W.make(s, micro_batches=1, with_dy=True)
+    L = layer.from_workload(wl)
+    x, dy = wl.x[0].torch("cuda"), wl.dy[0].torch("cuda")
+    L.forward(x)
+    L.backward(x, dy, accumulate=False)
+    L.backward(x, dy, accumulate=True)
+    torch.cuda.synchronize()
+    check_no_device_error()
+    xs, dys = wl.x[0].f32, wl.dy[0].f32
+    W1, W3, W2 = wl.W1.f32, wl.W3.f32, wl.W2.f32
+    st = O.route(xs, wl.W_r, wl.bias, s.k, None)
+    assert_routing_equal(L.saved, st, s.T)
+    counts = np.bincount(st["ids"].ravel(), minlength=s.E)
+    assert counts.max() >= 60 * 128 - 128 and counts.max() >= 8 * counts.min()
+    toks = _sample(s.T, 48, 5)
+    outs = [O.token_outputs(t, xs, dys, wl.W_r, wl.bias, W1, W3, W2, st) for t in toks]
+    assert_close("dx[sampled]", L.dx[torch.from_numpy(toks).cuda()], np.stack([o["dx"] for o in outs]), TOL)
+    cols = np.concatenate([_sample(s.d_ff, 12, 6), [0, 255, 256, s.d_ff - 1]])
+    cols = np.unique(cols)
+    c = O.weight_grad_columns(xs, dys, W1, W3, W2, st, cols)
+    ci = torch.from_numpy(cols).cuda()
+    assert_close("dW1[:, :, cols]", L.grads["dW1"][:, :, ci], 2 * c["dW1"], TOL)
+    assert_close("dW3[:, :, cols]", L.grads["dW3"][:, :, ci], 2 * c["dW3"], TOL)
+    assert_close("dW2[:, cols, :]", L.grads["dW2"][:, ci, :], 2 * c["dW2"], TOL)
+
+
 def test_train_e16_four_micro_batches_sampled():
     s = W.WORKLOADS["train_e16_bf16"]
     wl = W.make(s)
