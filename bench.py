@@ -19,6 +19,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -202,9 +203,27 @@ def binding(flops: float, nbytes: float, seconds: float, tflops_peak: float, hbm
     return {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s", "frac": round(ach / hbm_peak, 4)}
 
 
+# headers every kernel source includes (device helpers, PTX wrappers, launch declarations)
+KERNEL_HEADERS = ("common.cuh", "tc_ptx.cuh", "internal.h")
+
+
+def _code_only(text: str) -> str:
+    """C/CUDA source with its comments removed and whitespace runs collapsed, so
+    that an edit of comments alone leaves the digest unchanged."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def source_digest(name: str) -> str:
-    path = os.path.join(ROOT, "routing_permute_grouped_router_gb300", "csrc", KERNEL_SOURCES.get(name, "gemm_tc.cu"))
-    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+    """sha256[:16] of the code of kernel `name`: its source file and the shared headers,
+    comments removed.  A committed ncu record counts only while this matches."""
+    csrc = os.path.join(ROOT, "routing_permute_grouped_router_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in (KERNEL_SOURCES.get(name, "gemm_tc.cu"),) + KERNEL_HEADERS:
+        h.update(f.encode())
+        h.update(_code_only(open(os.path.join(csrc, f), encoding="utf-8").read()).encode())
+    return h.hexdigest()[:16]
 
 
 def committed_profile(name: str, workload: str):

@@ -20,7 +20,8 @@
 // reads 32 KB of operands instead of the 48 KB a single-SM 128 x 256 tile
 // needs for half the work.  Up, down and dgrad x run three 64 KB stages of two
 // such steps behind one pair of barriers; dgrad h and wgrad, whose epilogues
-// stage inputs, run five 32 KB stages of one step.
+// stage inputs, run five 32 KB stages of one step when K is short and three
+// 64 KB stages of two steps when it is long (the _L modes).
 //   warp 0, one lane: TMA producer of this CTA's halves into the stage ring;
 //     the byte count of both CTAs lands on the first CTA's barrier;
 //   warp 1: allocates TMEM with its peer; in the first CTA one lane issues
@@ -30,8 +31,10 @@
 //     32-row x 32-column slice per warp into registers, the fused math runs
 //     there, results go to HBM by TMA; they release the accumulator on the
 //     first CTA's barrier.
-// Tiles are taken round-robin over the pairs from a list the kernel derives on
-// the device from offsets/counts, so the host never reads the routing outcome.
+// Tiles are dealt to the pairs from a list the kernel derives on the device
+// from offsets/counts, so the host never reads the routing outcome: round-robin,
+// or for wgrad over experts of very different sizes in host and guest groups
+// (see next_group).
 // Expert segments are 128-row aligned, so the second half of an expert's last
 // pair tile may lie outside the expert: it is computed and not stored.  Every
 // mbarrier wait is bounded (2 s); on expiry the kernel records DEV_TIMEOUT in
