@@ -73,7 +73,7 @@ enum Mode { M_UP = 0, M_DOWN = 1, M_DGRAD_H = 2, M_DGRAD_X = 3, M_WGRAD = 4, M_D
 // layers: three 64 KB stages of two k-blocks, two gradient boxes a warp).
 __host__ __device__ constexpr bool is_wgrad(int m) { return m == M_WGRAD || m == M_WGRAD_L; }
 // dgrad h likewise: M_DGRAD_H (five 32 KB stages, its a|b boxes double-buffered)
-// for short K, M_DGRAD_H_L for d >= 4096 (three 64 KB stages of two k-blocks,
+// for short K, M_DGRAD_H_L for d >= 2048 (three 64 KB stages of two k-blocks,
 // one a|b buffer a warp: a chunk's a and b are requested once the previous
 // chunk's da and db have left the buffer, behind a long mainloop).
 __host__ __device__ constexpr bool is_dgrad_h(int m) { return m == M_DGRAD_H || m == M_DGRAD_H_L; }
@@ -1175,8 +1175,8 @@ cudaError_t tc_ffn_bwd(const Shape& s, const FfnBwdArgs& b, uint32_t* err, cudaS
   a.o1 = static_cast<__nv_bfloat16*>(b.db);
   a.i0 = static_cast<const __nv_bfloat16*>(b.a);
   a.i1 = static_cast<const __nv_bfloat16*>(b.b);
-  // long K (d >= 4096): the wide-stage shape
-  cudaError_t e = s.d >= 4096 ? launch_mode<M_DGRAD_H_L>(mh, a, mp * (s.f / BN), KK_GEMM_DGRAD_H, st)
+  // long K (d >= 2048, at least 32 k-blocks a tile): the wide-stage shape
+  cudaError_t e = s.d >= 2048 ? launch_mode<M_DGRAD_H_L>(mh, a, mp * (s.f / BN), KK_GEMM_DGRAD_H, st)
                               : launch_mode<M_DGRAD_H>(mh, a, mp * (s.f / BN), KK_GEMM_DGRAD_H, st);
   if (e != cudaSuccess) return e;
   a.w0 = b.dW1;

@@ -25,7 +25,7 @@ SMALL = {
     "dropless_e32_small": LS("dropless_e32_small", 1500, 512, 256, 32, 4, 0.0, W.BF16, zipf_s=1.3),
     "train_e16_small": LS("train_e16_small", 700, 256, 512, 16, 2, 1.25, W.BF16, micro_batches=4, backward=True),
     "train_f32_small": LS("train_f32_small", 333, 64, 96, 5, 2, 1.0, W.F32, micro_batches=2, backward=True),
-    # d = 4096 selects the long-K dgrad h shape (three 64 KB stages, one a|b buffer a warp)
+    # d = 4096 (any d >= 2048) selects the long-K dgrad h shape (three 64 KB stages, one a|b buffer a warp)
     "wide_d4096": LS("wide_d4096", 400, 4096, 256, 4, 2, 1.25, W.BF16),
 }
 
@@ -76,7 +76,7 @@ def test_layer_forward(name):
 @pytest.mark.parametrize("name", ["train_e16_small", "train_f32_small", "top2_e8_small", "zipf_e64_small",
                                   "dropless_e32_small", "wide_d4096"])
 def test_layer_backward_with_accumulation(name):
-    """The dropless layer runs the long-K wgrad shape and the d = 4096 layer the
+    """The dropless layer runs the long-K wgrad shape and the d = 4096 layer (d >= 2048) the
     long-K dgrad h shape; the others the short-K shapes."""
     s = SMALL[name]
     nmb = max(s.micro_batches, 2)
