@@ -39,7 +39,7 @@ KERNEL_SOURCES = {
     "combine_bwd": "rows.cu", "dx_router": "rows.cu", "transpose_wr": "rows.cu", "dwr_reduce": "rows.cu",
     "router_topk": "router_tc.cu", "split_wr": "router_tc.cu", "slot_scan": "routing.cu",
     "slot_assign": "routing.cu", "dwr": "dwr_tc.cu", "split_dl": "dwr_tc.cu", "aux_loss": "aux_loss.cu",
-    "aux_grad": "aux_loss.cu",
+    "aux_grad": "aux_loss.cu", "router_logit_grad": "rows.cu",
 }
 
 
@@ -168,6 +168,10 @@ def algorithmic_work(s, N: int, accumulate: bool = True, n_sms: int = 152):
     hist = E * k * nb * 4
     dwr_blocks = max(1, d // (256 if Ep <= 64 else 128))  # CTAs of the router-weight gradient along d
     dwr_ranges = max(1, min(n_sms // dwr_blocks, ((T + 63) // 64 + 1) // 2))
+    # large bf16 layers take each kept row's g * dg from the dgrad h product (per row, a sum
+    # of dH * h per 256-column tile), so their combine backward only scatters g * dY
+    fused_dg = s.dtype == "bf16" and T * k * d * 2 >= (256 << 20)  # as the library decides
+    nt = f // 256
     return {
         "split_wr": (0, d * E * 4 + 3 * Ep * d * 2),
         "router_topk": (2 * T * d * E, T * d * es + d * E * 4 + T * k * 8 + T * E * 4),
@@ -177,10 +181,11 @@ def algorithmic_work(s, N: int, accumulate: bool = True, n_sms: int = 152):
         "gemm_up_swiglu": (4 * N * d * f, N * d * es + 2 * Wb + 3 * N * f * es),
         "gemm_down": (2 * N * f * d, N * f * es + Wb + N * d * es),
         "unpermute_combine": (0, N * d * es + T * d * es),
-        "combine_bwd": (0, T * d * es + 2 * N * d * es + T * E * 4),
+        "combine_bwd": (0, T * d * es + N * d * es) if fused_dg else (0, T * d * es + 2 * N * d * es + T * E * 4),
+        "router_logit_grad": (0, N * nt * 4 + T * k * 12 + T * E * 4 * (2 if k == 1 else 1)),
         "aux_loss": (0, T * E * 4 + T * k * 4),
         "aux_grad": (0, 3 * T * E * 4),
-        "gemm_dgrad_h_swiglu_bwd": (2 * N * d * f, N * d * es + Wb + 4 * N * f * es),
+        "gemm_dgrad_h_swiglu_bwd": (2 * N * d * f, N * d * es + Wb + 4 * N * f * es + (N * nt * 4 if fused_dg else 0)),
         "gemm_wgrad": (6 * N * d * f, 2 * N * d * es + 3 * N * f * es + grad_rw),
         "gemm_dgrad_x": (4 * N * f * d, 2 * N * f * es + 2 * Wb + N * d * es),
         "transpose_wr": (0, 2 * d * E * 4),

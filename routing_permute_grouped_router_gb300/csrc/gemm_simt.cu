@@ -229,6 +229,7 @@ cudaError_t simt_ffn_fwd(const Shape& s, const FfnFwdArgs& f, uint32_t* err, cud
 }
 
 cudaError_t simt_ffn_bwd(const Shape& s, const FfnBwdArgs& b, uint32_t* err, cudaStream_t st) {
+  if (b.part != 0 || b.sdot != nullptr) return cudaErrorInvalidValue;  // the staged backward is bf16 only
   SimtArgs a{};
   a.x_perm = static_cast<const float*>(b.x_perm);
   a.a_in = static_cast<const float*>(b.a);

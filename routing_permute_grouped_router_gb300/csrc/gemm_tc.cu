@@ -148,6 +148,8 @@ struct TcArgs {
   const float* rdl;          // DGRAD_X, optional: logit gradient dl [T, E]; with it the row's
   const float* rwr;          //   router term dl[token, e] * W_r[:, e] is added (W_r [d, E])
   int rE;
+  float* sdot;  // DGRAD_H, optional: per row and column tile, sum over the tile's
+                // columns of dH * h ([max_rows, f / 256], h = silu(a) * b)
   int accumulate;
   uint32_t* err;
 };
@@ -589,6 +591,7 @@ __device__ __forceinline__ bool epilogue_tile(const TcMaps& maps, const TcArgs& 
     }
   } else if (is_dgrad_h(MODE)) {
     constexpr bool DOUBLE = ModeCfg<MODE>::ABUFS == 2;
+    float dot = 0.f;  // this lane's row: sum of dH * h over the tile's columns
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
       const uint32_t h = DOUBLE ? ((es.nbox + c) & 1) : 0u;
@@ -624,6 +627,10 @@ __device__ __forceinline__ bool epilogue_tile(const TcMaps& maps, const TcArgs& 
           dav[i] = dh * bv[i] * sg * (1.f + av[i] * (1.f - sg));
           dbv[i] = dh * av[i] * sg;
         }
+        if (a.sdot != nullptr) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) dot = fmaf(dbv[i], bv[i], dot);  // dH * silu(a) * b
+        }
         box_put_bf16x32(buf, lane, 4 * s, dav);
         box_put_bf16x32(buf + BOX_BYTES, lane, 4 * s, dbv);
       }
@@ -647,6 +654,7 @@ __device__ __forceinline__ bool epilogue_tile(const TcMaps& maps, const TcArgs& 
       }
     }
     es.nbox += 4;
+    if (a.sdot != nullptr) a.sdot[(int64_t)(row0 + lane) * (a.f / BN) + t.n0 / BN] = dot;
   } else if (wg_add) {  // WGRAD, accumulate: dW += acc via TMA load, add, TMA store
     // WG_BUFS buffers per warp; the old values of box c + WG_AHEAD are
     // requested while box c is added, so WG_AHEAD loads are in flight behind
@@ -1142,7 +1150,7 @@ cudaError_t tc_ffn_bwd(const Shape& s, const FfnBwdArgs& b, uint32_t* err, cudaS
   if (!resolve_encode()) return cudaErrorNotSupported;
   const uint64_t E = (uint64_t)s.E, d = (uint64_t)s.d, ff = (uint64_t)s.f;
   if (s.max_rows == 0) {
-    if (b.accumulate) return cudaSuccess;
+    if (b.accumulate || b.part == 1) return cudaSuccess;
     cudaError_t e = cudaMemsetAsync(b.dW1, 0, E * d * ff * 4, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(b.dW3, 0, E * d * ff * 4, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(b.dW2, 0, E * d * ff * 4, st);
@@ -1175,10 +1183,15 @@ cudaError_t tc_ffn_bwd(const Shape& s, const FfnBwdArgs& b, uint32_t* err, cudaS
   a.o1 = static_cast<__nv_bfloat16*>(b.db);
   a.i0 = static_cast<const __nv_bfloat16*>(b.a);
   a.i1 = static_cast<const __nv_bfloat16*>(b.b);
-  // long K (d >= 2048, at least 32 k-blocks a tile): the wide-stage shape
-  cudaError_t e = s.d >= 2048 ? launch_mode<M_DGRAD_H_L>(mh, a, mp * (s.f / BN), KK_GEMM_DGRAD_H, st)
-                              : launch_mode<M_DGRAD_H>(mh, a, mp * (s.f / BN), KK_GEMM_DGRAD_H, st);
-  if (e != cudaSuccess) return e;
+  a.sdot = b.sdot;
+  cudaError_t e = cudaSuccess;
+  if (b.part != 2) {
+    // long K (d >= 2048, at least 32 k-blocks a tile): the wide-stage shape
+    e = s.d >= 2048 ? launch_mode<M_DGRAD_H_L>(mh, a, mp * (s.f / BN), KK_GEMM_DGRAD_H, st)
+                    : launch_mode<M_DGRAD_H>(mh, a, mp * (s.f / BN), KK_GEMM_DGRAD_H, st);
+    if (e != cudaSuccess || b.part == 1) return e;
+  }
+  a.sdot = nullptr;
   a.w0 = b.dW1;
   a.w1 = b.dW3;
   a.w2 = b.dW2;

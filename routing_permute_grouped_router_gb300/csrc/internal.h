@@ -30,6 +30,7 @@ enum KernelKind : int {
   KK_SPLIT_DL,
   KK_AUX_LOSS,
   KK_AUX_GRAD,
+  KK_LOGIT_GRAD,
   KK_COUNT
 };
 
@@ -94,6 +95,12 @@ cudaError_t launch_combine_bwd(const Shape& s, const void* dy, const void* y_per
                                const int32_t* row_of, const float* gates, const float* probs,
                                const int32_t* counts, const int32_t* offsets, void* dy_perm, float* dg, float* dl,
                                uint32_t* err, cudaStream_t st);
+// dg and dl may be null: then only dy_perm = g * dy is written (y_perm unread)
+// dl [T, E] from the dgrad h product's per-row, per-256-column-tile sums of
+// dH * h (sdot [max_rows, nt]); overwrites dl
+cudaError_t launch_dl_from_dots(const Shape& s, const float* sdot, int nt, const int32_t* row_of,
+                                const int32_t* ids, const float* gates, const float* probs, float* dl, uint32_t* err,
+                                cudaStream_t st);
 // With ids given (skip_kept), the router terms of the token's kept experts are
 // taken to be in dx_perm already and only the other experts' terms are added.
 cudaError_t launch_dx_router(const Shape& s, const void* dx_perm, const int32_t* row_of, const float* dl,
@@ -138,6 +145,11 @@ struct FfnBwdArgs {
   // bf16 only, optional: with rdl (dl [T, E]), rwr (W_r [d, E]) and src_token
   // set, dx_perm[row] also holds the row's router term dl[token, e] * W_r[:, e]
   const float* rdl = nullptr; const float* rwr = nullptr; const int32_t* src_token = nullptr;
+  // bf16 only, optional: per row and 256-column tile of dH, the sum of dH * h
+  // ([max_rows, f / 256] fp32), written by the dgrad h product
+  float* sdot = nullptr;
+  // bf16 only: 0 runs dgrad h, wgrad and dgrad x; 1 dgrad h alone; 2 wgrad and dgrad x
+  int part = 0;
 };
 cudaError_t tc_ffn_fwd(const Shape& s, const FfnFwdArgs& a, uint32_t* err, cudaStream_t st);
 cudaError_t tc_ffn_bwd(const Shape& s, const FfnBwdArgs& a, uint32_t* err, cudaStream_t st);

@@ -83,7 +83,7 @@ const char* const kKernelNames[KK_COUNT] = {
     "router_topk",  "slot_scan",  "slot_assign",     "permute",      "gemm_up_swiglu", "gemm_down",
     "unpermute_combine", "combine_bwd", "gemm_dgrad_h_swiglu_bwd", "gemm_wgrad", "gemm_dgrad_x",
     "transpose_wr", "dx_router",  "dwr",     "dwr_reduce",   "zero", "split_wr", "selftest_bounded_wait",
-    "split_dl", "aux_loss", "aux_grad"};
+    "split_dl", "aux_loss", "aux_grad", "router_logit_grad"};
 
 }  // namespace
 
@@ -211,9 +211,16 @@ struct FwdScratch {
   void *x_perm, *h, *y_perm;
   float* row_gate;  // gate of each row (inference forward with the combine in the down product)
 };
+// The layer backward takes dg from the dgrad h product (and skips reading Y_perm
+// back in the combine backward) when the Y_perm bytes saved, up to T k d of
+// bf16, are at least 256 MB; below that the extra launch costs more than the
+// read it saves (top-2 E=8 layer: +6 us a step; dropless E=32: -170 us).
+bool fused_dg_pays(const Shape& s) { return s.bf16 && (int64_t)s.T * s.k * s.d * 2 >= ((int64_t)256 << 20); }
+
 struct BwdScratch {
   void *dy_perm, *da, *db, *dx_perm;
   float *dg, *dl, *W_rT, *partial;
+  float* sdot;    // bf16: per row and 256-column tile, sum of dH * h (the layer backward's dg * g)
   void* dlsplit;  // bf16 parts of dl for the tensor-core router-weight gradient
   void* aux;      // auxiliary-loss partial sums
 };
@@ -258,6 +265,7 @@ BwdScratch carve_bwd(Carver& c, const Shape& s) {
   b.partial = static_cast<float*>(c.take((size_t)(tc ? dwr_tc_ranges(s) : dwr_splits(s)) * s.d * s.E * 4));
   b.dlsplit = c.take(tc ? dwr_tc_split_bytes(s) : 0);
   b.aux = c.take(aux_scratch_bytes(s));
+  b.sdot = static_cast<float*>(c.take(fused_dg_pays(s) ? R * (size_t)(s.f / 256) * 4 : 0));
   return b;
 }
 // a, b, h of the expert FFN when the forward does not keep them (the
@@ -313,7 +321,7 @@ moe_status do_ffn_fwd(const Shape& s, const FfnFwdArgs& f, uint32_t* err, cudaSt
 
 moe_status do_ffn_bwd(const Shape& s, const FfnBwdArgs& b, uint32_t* err, cudaStream_t st) {
   if (s.max_rows == 0 || s.T == 0) {
-    if (b.accumulate) return MOE_OK;
+    if (b.accumulate || b.part == 1) return MOE_OK;
     const size_t n = (size_t)s.E * s.d * s.f * 4;
     CUDA_TRY(cudaMemsetAsync(b.dW1, 0, n, st));
     CUDA_TRY(cudaMemsetAsync(b.dW3, 0, n, st));
@@ -680,21 +688,35 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* w, const void
     act_b = rc.b;
     act_h = rc.h;
   }
-  if (s.T > 0)
-    CUDA_TRY(launch_combine_bwd(s, dy, saved->y_perm, saved->ids, saved->row_of, saved->gates, saved->probs,
-                                saved->counts, saved->offsets, bs.dy_perm, bs.dg, bs.dl, err, stream));
-  CUDA_TRY(launch_aux_loss(s, s.aux, saved->probs, saved->ids, grads->aux_loss, bs.dl, bs.aux, err, stream));
-  FfnBwdArgs fb{saved->x_perm, act_a, act_b, act_h, bs.dy_perm, saved->counts, saved->offsets,
-                w->W1, w->W3, w->W2, bs.da, bs.db, bs.dx_perm, grads->dW1, grads->dW3, grads->dW2, accumulate};
   // bf16 layers: the router term of each kept row, dl[t, e] W_r[:, e], is added
   // in the dgrad x epilogue (its expert is the tile's), so the dx gather adds
-  // only the terms of the experts a token does not keep a row for
+  // only the terms of the experts a token does not keep a row for.  Large bf16
+  // layers also take each kept row's g * dg = <g dY W2^T, h> = <dH, h> from the
+  // dgrad h epilogue, so the combine backward only scatters g * dY (Y_perm is not
+  // read back) and the logit gradient dl follows the dgrad h product.
   const bool fuse_router = s.bf16 != 0;
+  const bool fuse_dg = fuse_router && fused_dg_pays(s);
+  if (s.T > 0)
+    CUDA_TRY(launch_combine_bwd(s, dy, saved->y_perm, saved->ids, saved->row_of, saved->gates, saved->probs,
+                                saved->counts, saved->offsets, bs.dy_perm, fuse_dg ? nullptr : bs.dg,
+                                fuse_dg ? nullptr : bs.dl, err, stream));
+  FfnBwdArgs fb{saved->x_perm, act_a, act_b, act_h, bs.dy_perm, saved->counts, saved->offsets,
+                w->W1, w->W3, w->W2, bs.da, bs.db, bs.dx_perm, grads->dW1, grads->dW3, grads->dW2, accumulate};
   if (fuse_router) {
     fb.rdl = bs.dl;
     fb.rwr = w->W_r;
     fb.src_token = saved->src_token;
   }
+  if (fuse_dg) {
+    fb.sdot = bs.sdot;
+    fb.part = 1;  // dgrad h
+    MOE_TRY(do_ffn_bwd(s, fb, err, stream));
+    CUDA_TRY(launch_dl_from_dots(s, bs.sdot, s.f / 256, saved->row_of, saved->ids, saved->gates, saved->probs,
+                                 bs.dl, err, stream));
+    fb.sdot = nullptr;
+    fb.part = 2;  // wgrad and dgrad x
+  }
+  CUDA_TRY(launch_aux_loss(s, s.aux, saved->probs, saved->ids, grads->aux_loss, bs.dl, bs.aux, err, stream));
   MOE_TRY(do_ffn_bwd(s, fb, err, stream));
   return do_dx_router(s, x, bs.dx_perm, saved->row_of, bs.dl, w->W_r, dx, grads->dW_r, accumulate, bs, err, stream,
                       fuse_router ? saved->ids : nullptr);

@@ -195,11 +195,14 @@ struct CombBwdArgs {
   int token_blocks;
 };
 
-template <typename Tx, int K>
+// DG: also dg = <dY[t], Y_perm[row]> and dl from it; without DG only the
+// scatter dY_perm = g * dY (the layer backward of bf16 layers takes dg * g
+// from the dgrad h product instead, see dl_from_dots_kernel)
+template <typename Tx, int K, bool DG>
 __global__ void __launch_bounds__(RW_WARPS * 32) combine_bwd_kernel(CombBwdArgs a) {
   pdl_enter();  // see pdl_wait: no global access before this
   constexpr int VN = Vec<Tx>::N;
-  constexpr int U = INFLIGHT / (K + 1) > 0 ? INFLIGHT / (K + 1) : 1;
+  constexpr int U = !DG ? INFLIGHT : (INFLIGHT / (K + 1) > 0 ? INFLIGHT / (K + 1) : 1);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if ((int)blockIdx.x >= a.token_blocks) {
     zero_pad_rows(a.counts, a.offsets, blockIdx.x - a.token_blocks, a.dy_perm, a.nvec, a.max_rows, a.err, warp,
@@ -226,13 +229,15 @@ __global__ void __launch_bounds__(RW_WARPS * 32) combine_bwd_kernel(CombBwdArgs 
       const int v = v0 + lane + 32 * u;
       dyb[u] = v < a.nvec ? ldg16(src + v * 16) : make_uint4(0, 0, 0, 0);
     }
+    if constexpr (DG) {
 #pragma unroll
-    for (int j = 0; j < K; ++j)
+      for (int j = 0; j < K; ++j)
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int v = v0 + lane + 32 * u;
-        yb[j][u] = (rows[j] >= 0 && v < a.nvec) ? ldg16(yp + (rows[j] * a.nvec + v) * 16) : make_uint4(0, 0, 0, 0);
-      }
+        for (int u = 0; u < U; ++u) {
+          const int v = v0 + lane + 32 * u;
+          yb[j][u] = (rows[j] >= 0 && v < a.nvec) ? ldg16(yp + (rows[j] * a.nvec + v) * 16) : make_uint4(0, 0, 0, 0);
+        }
+    }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int v = v0 + lane + 32 * u;
@@ -242,17 +247,20 @@ __global__ void __launch_bounds__(RW_WARPS * 32) combine_bwd_kernel(CombBwdArgs 
 #pragma unroll
       for (int j = 0; j < K; ++j) {
         if (rows[j] < 0) continue;
-        float yv[VN], o[VN];
-        unpack(yb[j][u], yv);
+        float o[VN];
+        if constexpr (DG) {
+          float yv[VN];
+          unpack(yb[j][u], yv);
 #pragma unroll
-        for (int i = 0; i < VN; ++i) {
-          part[j] = fmaf(dyv[i], yv[i], part[j]);
-          o[i] = g[j] * dyv[i];
+          for (int i = 0; i < VN; ++i) part[j] = fmaf(dyv[i], yv[i], part[j]);
         }
+#pragma unroll
+        for (int i = 0; i < VN; ++i) o[i] = g[j] * dyv[i];
         stg16(out + (rows[j] * a.nvec + v) * 16, pack(o));
       }
     }
   }
+  if constexpr (!DG) return;
   float dg[K];
   float s = 0.f;
 #pragma unroll
@@ -303,6 +311,72 @@ __global__ void transpose_wr_kernel(const float* W_r, float* W_rT, int d, int E)
   for (int r = threadIdx.y; r < 32; r += 8) {
     const int e = e0 + r, i = i0 + threadIdx.x;
     if (e < E && i < d) W_rT[(size_t)e * d + i] = tile[threadIdx.x][r];
+  }
+}
+
+// -------------------------------------------------------------------------- //
+// Router logit gradient from the dgrad h product's row sums.  For a kept row,
+// g * dg = g <dY[t], Y_perm[row]> = <g dY[t] W2^T, h[row]> = <dH[row], h[row]>,
+// which the dgrad h epilogue has summed per 256-column tile (sdot); with
+// s_j = g_j dg_j (0 for a dropped pick) the softmax-over-picks Jacobian gives
+// dl[t, e_j] = s_j - g_j sum_i s_i for k > 1 and dl[t, e] = s (onehot - p[e])
+// for k = 1 ("The step timeline", gpu_expert_parallel page: the backward walks
+// the path in reverse; the router's logits are the gates' parameters).
+// -------------------------------------------------------------------------- //
+struct DotArgs {
+  const float* sdot;  // [max_rows, nt]
+  const int32_t* row_of;
+  const int32_t* ids;
+  const float* gates;
+  const float* probs;  // [T, E], k = 1
+  float* dl;           // [T, E]
+  uint32_t* err;
+  int T, E, nt;
+  int64_t max_rows;
+};
+
+template <int K>
+__global__ void __launch_bounds__(RW_WARPS * 32) dl_from_dots_kernel(DotArgs a) {
+  pdl_enter();  // see pdl_wait: no global access before this
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int t = blockIdx.x * RW_WARPS + warp;
+  if (t >= a.T) return;
+  int64_t rows[K];
+  load_rows<K>(a.row_of, t, a.max_rows, a.err, lane, 15, rows);
+  // every pick's loads first, then the K butterfly sums side by side (a fixed
+  // reduction order: the same bits every run)
+  float sj[K], g[K];
+#pragma unroll
+  for (int j = 0; j < K; ++j) {
+    g[j] = a.gates[(size_t)t * K + j];
+    sj[j] = 0.f;
+    if (rows[j] >= 0)
+      for (int n = lane; n < a.nt; n += 32) sj[j] += a.sdot[rows[j] * a.nt + n];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int j = 0; j < K; ++j) sj[j] += __shfl_xor_sync(0xffffffffu, sj[j], o);
+  float S = 0.f;
+#pragma unroll
+  for (int j = 0; j < K; ++j) S += sj[j];
+  if (K == 1) {
+    const int e1 = a.ids[(size_t)t];
+    for (int e = lane; e < a.E; e += 32) {
+      const float p = a.probs[(size_t)t * a.E + e];
+      a.dl[(size_t)t * a.E + e] = sj[0] * ((e == e1 ? 1.f : 0.f) - p);
+    }
+  } else {
+    int ids[K];
+#pragma unroll
+    for (int j = 0; j < K; ++j) ids[j] = a.ids[(size_t)t * K + j];
+    for (int e = lane; e < a.E; e += 32) {
+      float v = 0.f;
+#pragma unroll
+      for (int j = 0; j < K; ++j)
+        if (ids[j] == e) v += sj[j] - g[j] * S;
+      a.dl[(size_t)t * a.E + e] = v;
+    }
   }
 }
 
@@ -641,7 +715,14 @@ struct CombineL {
 template <typename Tx, int K>
 struct CombineBwdL {
   static cudaError_t launch(const CombBwdArgs& a, int grid, cudaStream_t st) {
-    return launch_pdl(combine_bwd_kernel<Tx, K>, dim3(grid), dim3(RW_WARPS * 32), 0, st, a);
+    if (a.dg == nullptr) return launch_pdl(combine_bwd_kernel<Tx, K, false>, dim3(grid), dim3(RW_WARPS * 32), 0, st, a);
+    return launch_pdl(combine_bwd_kernel<Tx, K, true>, dim3(grid), dim3(RW_WARPS * 32), 0, st, a);
+  }
+};
+template <typename Tx, int K>
+struct DotL {  // no activation data: the element type does not matter
+  static cudaError_t launch(const DotArgs& a, int grid, cudaStream_t st) {
+    return launch_pdl(dl_from_dots_kernel<K>, dim3(grid), dim3(RW_WARPS * 32), 0, st, a);
   }
 };
 template <typename Tx, int K>
@@ -686,6 +767,15 @@ cudaError_t launch_combine_bwd(const Shape& s, const void* dy, const void* y_per
                 (s.T + RW_WARPS - 1) / RW_WARPS};
   LaunchScope ls(KK_COMBINE_BWD, st);
   return launch_typed_k<CombineBwdL>(s, a, a.token_blocks + s.E, st);
+}
+
+cudaError_t launch_dl_from_dots(const Shape& s, const float* sdot, int nt, const int32_t* row_of,
+                                const int32_t* ids, const float* gates, const float* probs, float* dl, uint32_t* err,
+                                cudaStream_t st) {
+  if (s.T == 0) return cudaSuccess;
+  DotArgs a{sdot, row_of, ids, gates, probs, dl, err, s.T, s.E, nt, s.max_rows};
+  LaunchScope ls(KK_LOGIT_GRAD, st);
+  return launch_typed_k<DotL>(s, a, (s.T + RW_WARPS - 1) / RW_WARPS, st);
 }
 
 cudaError_t launch_dx_router(const Shape& s, const void* dx_perm, const int32_t* row_of, const float* dl,

@@ -130,6 +130,28 @@ def test_dropless_e32_full_backward_sampled():
     assert_close("dW2[:, cols, :]", L.grads["dW2"][:, ci, :], 2 * c["dW2"], TOL)
 
 
+def test_large_layer_logit_gradient_from_the_dgrad_h_product():
+    """A bf16 layer whose Y_perm would be at least 256 MB (T k d = 2^27) takes each kept
+    row's g * dg from the dgrad h epilogue instead of reading Y_perm back: the logit
+    gradient reaches dx (router term) and dW_r, compared whole with the oracle."""
+    s = W.LayerShape("fused_dg", 16384, 2048, 256, 8, 4, 0.0, W.BF16)
+    assert s.T * s.k * s.d_model * 2 >= 256 << 20
+    wl = W.make(s, micro_batches=1, with_dy=True)
+    L = layer.from_workload(wl)
+    x, dy = wl.x[0].torch("cuda"), wl.dy[0].torch("cuda")
+    L.forward(x)
+    L.backward(x, dy, accumulate=False)
+    torch.cuda.synchronize()
+    check_no_device_error()
+    st = O.forward(wl.x[0].f64(), wl.W_r, wl.bias, wl.W1.f64(), wl.W3.f64(), wl.W2.f64(), s.k, _cap(s))
+    gr = O.backward(wl.dy[0].f64(), wl.x[0].f64(), wl.W_r, wl.W1.f64(), wl.W3.f64(), wl.W2.f64(), st)
+    assert_routing_equal(L.saved, st, s.T)
+    assert_close("y", L.y, st["y"], TOL)
+    assert_close("dx", L.dx, gr["dx"], TOL)
+    for n in ("dW_r", "dW1", "dW3", "dW2"):
+        assert_close(n, L.grads[n], gr[n], TOL)
+
+
 def test_dropless_skewed_wgrad_host_and_guest_tiles_sampled():
     """wgrad with interleaved host and guest tiles away from the benchmark shape.
 
