@@ -335,42 +335,49 @@ struct DotArgs {
   int64_t max_rows;
 };
 
+// Eight lanes a token, four tokens a warp (the per-token work is small: k row
+// sums of f / 256 values and E outputs).
 template <int K>
 __global__ void __launch_bounds__(RW_WARPS * 32) dl_from_dots_kernel(DotArgs a) {
   pdl_enter();  // see pdl_wait: no global access before this
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int t = blockIdx.x * RW_WARPS + warp;
-  if (t >= a.T) return;
-  int64_t rows[K];
-  load_rows<K>(a.row_of, t, a.max_rows, a.err, lane, 15, rows);
-  // every pick's loads first, then the K butterfly sums side by side (a fixed
-  // reduction order: the same bits every run)
+  const int u = lane & 7;  // lane within the token's group of eight
+  const int t = (blockIdx.x * RW_WARPS + warp) * 4 + (lane >> 3);
+  const bool live = t < a.T;  // every lane takes part in the shuffles below
   float sj[K], g[K];
+  int ids[K];
 #pragma unroll
   for (int j = 0; j < K; ++j) {
-    g[j] = a.gates[(size_t)t * K + j];
     sj[j] = 0.f;
-    if (rows[j] >= 0)
-      for (int n = lane; n < a.nt; n += 32) sj[j] += a.sdot[rows[j] * a.nt + n];
+    g[j] = 0.f;
+    ids[j] = -1;
+    if (!live) continue;
+    const int64_t r = a.row_of[(size_t)t * K + j];
+    g[j] = a.gates[(size_t)t * K + j];
+    ids[j] = a.ids[(size_t)t * K + j];
+    if (r >= 0 && !row_ok(r, a.max_rows)) {
+      if (u == 0) report_error(a.err, DEV_BAD_ROW, 15);
+    } else if (r >= 0) {
+      for (int n = u; n < a.nt; n += 8) sj[j] += a.sdot[r * a.nt + n];
+    }
   }
+  // the group's eight partial sums of each pick, by a fixed butterfly (the same
+  // bits every run)
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1)
+  for (int o = 4; o > 0; o >>= 1)
 #pragma unroll
     for (int j = 0; j < K; ++j) sj[j] += __shfl_xor_sync(0xffffffffu, sj[j], o);
+  if (!live) return;
   float S = 0.f;
 #pragma unroll
   for (int j = 0; j < K; ++j) S += sj[j];
   if (K == 1) {
-    const int e1 = a.ids[(size_t)t];
-    for (int e = lane; e < a.E; e += 32) {
+    for (int e = u; e < a.E; e += 8) {
       const float p = a.probs[(size_t)t * a.E + e];
-      a.dl[(size_t)t * a.E + e] = sj[0] * ((e == e1 ? 1.f : 0.f) - p);
+      a.dl[(size_t)t * a.E + e] = sj[0] * ((e == ids[0] ? 1.f : 0.f) - p);
     }
   } else {
-    int ids[K];
-#pragma unroll
-    for (int j = 0; j < K; ++j) ids[j] = a.ids[(size_t)t * K + j];
-    for (int e = lane; e < a.E; e += 32) {
+    for (int e = u; e < a.E; e += 8) {
       float v = 0.f;
 #pragma unroll
       for (int j = 0; j < K; ++j)
@@ -775,7 +782,7 @@ cudaError_t launch_dl_from_dots(const Shape& s, const float* sdot, int nt, const
   if (s.T == 0) return cudaSuccess;
   DotArgs a{sdot, row_of, ids, gates, probs, dl, err, s.T, s.E, nt, s.max_rows};
   LaunchScope ls(KK_LOGIT_GRAD, st);
-  return launch_typed_k<DotL>(s, a, (s.T + RW_WARPS - 1) / RW_WARPS, st);
+  return launch_typed_k<DotL>(s, a, (s.T + 4 * RW_WARPS - 1) / (4 * RW_WARPS), st);
 }
 
 cudaError_t launch_dx_router(const Shape& s, const void* dx_perm, const int32_t* row_of, const float* dl,
