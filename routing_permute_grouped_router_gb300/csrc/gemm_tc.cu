@@ -150,6 +150,8 @@ struct TcArgs {
   int rE;
   float* sdot;  // DGRAD_H, optional: per row and column tile, sum over the tile's
                 // columns of dH * h ([max_rows, f / 256], h = silu(a) * b)
+  int* round_ctr;  // WGRAD, optional: zeroed counters, one a round of host and guest
+                   // tiles, that keep the pairs' rounds in step (WG_ROUNDS of them)
   int accumulate;
   uint32_t* err;
 };
@@ -253,6 +255,7 @@ __device__ __forceinline__ int n_tiles_of(const TcArgs& a) {
 // host: one guest per GUEST_GAP stages, with at least GUEST_GAP stages of the
 // host after the last guest), and guests have at most GUEST_MAX stages.
 struct Group {
+  int members;  // pairs with a group in this round (interleaving)
   int host;   // tile index of the host
   int g;      // guests
   int gbase;  // guest i is tile gbase - i
@@ -295,6 +298,7 @@ __device__ __forceinline__ bool next_group(GroupIter& it, Group& gr, int pair, i
     if (g < 0) g = 0;
   }
   const int F0 = it.F, B0 = it.B;
+  gr.members = left < npairs ? left : npairs;
   it.F += npairs;
   it.B -= g * npairs;
   if (pair >= (left < npairs ? left : npairs)) return false;
@@ -847,7 +851,27 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_kernel(const __grid_consta
       };
       GroupIter it{0, total, 0};
       Group gr;
+      int rnd = 0;
       while (alive && next_group<MODE>(it, gr, pair, npairs, total, interleave, a, s_cnt, s_pair)) {
+        // Keep the rounds of host and guest tiles in step: the tiles running
+        // together share operand panels through L2 only while they walk K
+        // together, and after a round that straddles experts of different sizes
+        // the pairs would otherwise drift apart for the rest of the launch.
+        // Every producer of the round arrives on the round's counter and waits
+        // (bounded) for the others; all CTAs are resident, one an SM.
+        if (is_wgrad(MODE) && interleave && a.round_ctr != nullptr && rnd > 0 && rnd < WG_ROUNDS) {
+          atomicAdd(&a.round_ctr[rnd], 1);
+          const int need = 2 * gr.members;
+          const uint64_t t0 = globaltimer();
+          while (*reinterpret_cast<volatile int*>(&a.round_ctr[rnd]) < need) {
+            if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+              report_error(a.err, DEV_TIMEOUT, 190 + MODE);
+              break;
+            }
+            __nanosleep(128);
+          }
+        }
+        ++rnd;
         const Tile th = decode<MODE>(gr.host, rank, a, s_off, s_cnt, s_pair);
         int hk = 0;
         for (int i = 0; i <= gr.g && alive; ++i) {
@@ -1197,8 +1221,15 @@ cudaError_t tc_ffn_bwd(const Shape& s, const FfnBwdArgs& b, uint32_t* err, cudaS
   a.w2 = b.dW2;
   // long K per tile (dropless, or a capacity above 2048 rows): the wide-stage shape
   const int64_t wg_tiles = (int64_t)s.E * 3 * (s.d / (2 * BM)) * (s.f / BN);
-  if (s.cap > 2048)
+  if (s.cap > 2048) {
+    if (b.round_ctr != nullptr) {
+      e = cudaMemsetAsync(b.round_ctr, 0, sizeof(int) * WG_ROUNDS, st);
+      if (e != cudaSuccess) return e;
+      a.round_ctr = b.round_ctr;
+    }
     e = launch_mode<M_WGRAD_L>(mw, a, wg_tiles, KK_GEMM_WGRAD, st);
+    a.round_ctr = nullptr;
+  }
   else
     e = launch_mode<M_WGRAD>(mw, a, wg_tiles, KK_GEMM_WGRAD, st);
   if (e != cudaSuccess) return e;

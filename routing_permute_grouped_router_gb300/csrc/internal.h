@@ -150,7 +150,11 @@ struct FfnBwdArgs {
   float* sdot = nullptr;
   // bf16 only: 0 runs dgrad h, wgrad and dgrad x; 1 dgrad h alone; 2 wgrad and dgrad x
   int part = 0;
+  // bf16 only, optional: WG_ROUNDS ints of scratch (zeroed by the call) with which
+  // wgrad keeps its rounds of host and guest tiles in step
+  int* round_ctr = nullptr;
 };
+constexpr int WG_ROUNDS = 4096;  // rounds of host and guest tiles kept in step (later ones run free)
 cudaError_t tc_ffn_fwd(const Shape& s, const FfnFwdArgs& a, uint32_t* err, cudaStream_t st);
 cudaError_t tc_ffn_bwd(const Shape& s, const FfnBwdArgs& a, uint32_t* err, cudaStream_t st);
 cudaError_t simt_ffn_fwd(const Shape& s, const FfnFwdArgs& a, uint32_t* err, cudaStream_t st);

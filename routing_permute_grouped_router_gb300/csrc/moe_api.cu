@@ -221,6 +221,7 @@ struct BwdScratch {
   void *dy_perm, *da, *db, *dx_perm;
   float *dg, *dl, *W_rT, *partial;
   float* sdot;    // bf16: per row and 256-column tile, sum of dH * h (the layer backward's dg * g)
+  int* round_ctr;  // bf16: wgrad's round counters
   void* dlsplit;  // bf16 parts of dl for the tensor-core router-weight gradient
   void* aux;      // auxiliary-loss partial sums
 };
@@ -266,6 +267,7 @@ BwdScratch carve_bwd(Carver& c, const Shape& s) {
   b.dlsplit = c.take(tc ? dwr_tc_split_bytes(s) : 0);
   b.aux = c.take(aux_scratch_bytes(s));
   b.sdot = static_cast<float*>(c.take(fused_dg_pays(s) ? R * (size_t)(s.f / 256) * 4 : 0));
+  b.round_ctr = static_cast<int*>(c.take(s.bf16 ? sizeof(int) * WG_ROUNDS : 0));
   return b;
 }
 // a, b, h of the expert FFN when the forward does not keep them (the
@@ -702,6 +704,7 @@ moe_status moe_layer_bwd(const moe_config* cfg, const moe_weights* w, const void
                                 fuse_dg ? nullptr : bs.dl, err, stream));
   FfnBwdArgs fb{saved->x_perm, act_a, act_b, act_h, bs.dy_perm, saved->counts, saved->offsets,
                 w->W1, w->W3, w->W2, bs.da, bs.db, bs.dx_perm, grads->dW1, grads->dW3, grads->dW2, accumulate};
+  fb.round_ctr = bs.round_ctr;
   if (fuse_router) {
     fb.rdl = bs.dl;
     fb.rwr = w->W_r;
