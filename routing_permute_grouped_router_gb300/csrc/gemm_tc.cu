@@ -427,11 +427,18 @@ __device__ __forceinline__ void stage_wait(int lane) {
   if (lane == 0) bulk_wait_read1();
   __syncwarp();
 }
-__device__ __forceinline__ void box_issue_store(const CUtensorMap* map, uint32_t buf, int c0, int c1, int lane) {
+// bf16 results go out with an L2 evict-first policy (they are read back only by
+// a later kernel, after far more data has passed through L2), which keeps the
+// operand panels and weights in L2 a little longer (4-micro-batch E=16 step
+// -0.4 %, 0.3 GB less DRAM traffic a dropless E=32 step); wgrad's fp32 gradient
+// boxes use the default policy (evict-first there was slower)
+__device__ __forceinline__ void box_issue_store(const CUtensorMap* map, uint32_t buf, int c0, int c1, int lane,
+                                                bool first = true) {
   fence_async_smem();
   __syncwarp();
   if (lane == 0) {
-    tma_store_2d(map, buf, c0, c1);
+    if (first) tma_store_2d_hint(map, buf, c0, c1, l2_evict_first_policy());
+    else tma_store_2d(map, buf, c0, c1);
     bulk_commit();
   }
 }
@@ -641,8 +648,8 @@ __device__ __forceinline__ bool epilogue_tile(const TcMaps& maps, const TcArgs& 
       fence_async_smem();
       __syncwarp();
       if (lane == 0) {
-        tma_store_2d(&maps.m[4], buf, t.n0 + c * 64, row0);
-        tma_store_2d(&maps.m[5], buf + BOX_BYTES, t.n0 + c * 64, row0);
+        tma_store_2d_hint(&maps.m[4], buf, t.n0 + c * 64, row0, l2_evict_first_policy());
+        tma_store_2d_hint(&maps.m[5], buf + BOX_BYTES, t.n0 + c * 64, row0, l2_evict_first_policy());
         bulk_commit();
       }
       if (!DOUBLE && c + 1 < 4) {
@@ -692,7 +699,7 @@ __device__ __forceinline__ bool epilogue_tile(const TcMaps& maps, const TcArgs& 
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = old[i] + __uint_as_float(r[i]);
       box_put_f32x32(buf, lane, v);
-      box_issue_store(wg_map, buf, t.n0 + c * 32, wg_orow, lane);
+      box_issue_store(wg_map, buf, t.n0 + c * 32, wg_orow, lane, false);
     }
     es.nbox += 8;
   } else {  // WGRAD, overwrite (or an expert with no rows and accumulate = 0)
@@ -712,7 +719,7 @@ __device__ __forceinline__ bool epilogue_tile(const TcMaps& maps, const TcArgs& 
         for (int i = 0; i < 32; ++i) v[i] = 0.f;
       }
       box_put_f32x32(buf, lane, v);
-      box_issue_store(wg_map, buf, t.n0 + c * 32, wg_orow, lane);
+      box_issue_store(wg_map, buf, t.n0 + c * 32, wg_orow, lane, false);
       ++es.nbox;
     }
   }
