@@ -213,8 +213,9 @@ struct FwdScratch {
 };
 // The layer backward takes dg from the dgrad h product (and skips reading Y_perm
 // back in the combine backward) when the Y_perm bytes saved, up to T k d of
-// bf16, are at least 256 MB; below that the extra launch costs more than the
-// read it saves (top-2 E=8 layer: +6 us a step; dropless E=32: -170 us).
+// bf16, are at least 256 MB; below that the extra launch costs about as much
+// as the read it saves or more (top-2 E=8 layer: +6 us a step; 4-micro-batch
+// E=16 and Zipf E=64: within 0.2 %; dropless E=32: -170 us).
 bool fused_dg_pays(const Shape& s) { return s.bf16 && (int64_t)s.T * s.k * s.d * 2 >= ((int64_t)256 << 20); }
 
 struct BwdScratch {
